@@ -1,0 +1,661 @@
+// Balanced persistent decode kernel for bf16 GQA groups of 4..16 q heads per kv head
+// (TMA page staging + mma.sync), and its split reduce.
+//
+// Work list. The unit of work is one (sequence, kv head, logical block) page: 16 tokens x
+// head_dim of K plus the same of V (8 KB at head_dim 128). Units are ordered sequence-major,
+// then kv head, then page, so the units of one (sequence, kv head) "segment" are contiguous.
+// Every CTA rebuilds the same list from seq_lens with a block-wide scan and takes an equal
+// contiguous slice; inside the CTA every warp takes an equal contiguous sub-slice. The grid
+// is one wave of persistent CTAs, and per-SM work differs by at most one page whatever the
+// mix of lengths.
+//
+// Streaming. Each warp is an independent worker with its own ring of stages in shared memory.
+// Lane 0 resolves the page's physical block through the block table ("My Understanding of
+// vLLM and PagedAttention", "Block Table"), then issues two 2-D TMA tile copies per 64-column
+// half (K and V, 128-byte swizzle) completing on the stage's mbarrier; when the unit starts a
+// new segment it also bulk-copies that segment's G query rows into the stage. Block ids are
+// fetched 32 units ahead by the warp's lanes. The warp consumes a stage (S = Q K^T and O += P V
+// on mma.sync m16n8k16, rows = the G q heads that share the kv head, so each page is read once
+// for the whole group; online softmax in registers, log2 domain) and refills it with the
+// unit `stages` ahead. The unused tail of a sequence's last block may hold anything: its keys
+// are masked to -inf and its V rows are zeroed in shared memory before P V.
+//
+// Merging. A segment that lies wholly inside a warp's sub-slice is normalised and written
+// from registers. Pieces of segments cut by sub-slice boundaries meet in shared memory after
+// one CTA barrier; segments cut by CTA boundaries leave (m, l, o) pieces in the workspace, and
+// the reduce kernel (launched with programmatic dependent launch, so its launch overlaps the
+// main kernel) merges them:  M = max m_p, w_p = l_p 2^(m_p - M), out = sum w_p o_p / sum w_p.
+#include <cuda.h>  // CUtensorMap (type only)
+#include <math.h>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kBalMaxGroup = 16;
+constexpr int kBalMaxSeqs = 1024;     // per-sequence tables live in shared memory
+constexpr int kBalMaxWarps = 2048;    // streaming warps in the grid (bounds the piece list)
+
+__host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+// Stage: K page (D/64 swizzled 2 KB boxes), V page, then the segment's query rows.
+__host__ __device__ inline uint32_t bal_stage_bytes(int D, int G) {
+    return align_up(2u * kBlock * D * 2u + static_cast<uint32_t>(G) * D * 2u, 1024u);
+}
+
+struct BalLayout {
+    uint32_t ring, bars, flags, prefix, lens, total;
+};
+
+__host__ __device__ inline BalLayout bal_layout(int NW, int nst, uint32_t stage_bytes, int S) {
+    BalLayout L;
+    uint32_t o = 0;
+    L.ring = o;    o += static_cast<uint32_t>(NW) * nst * stage_bytes;
+    L.bars = o;    o += static_cast<uint32_t>(NW) * nst * 8u;
+    L.flags = o;   o += 16u;
+    L.prefix = o;  o += align_up((S + 1) * 4u, 16u);
+    L.lens = o;    o += align_up(S * 4u, 16u);
+    L.total = o + 1024u;  // base alignment slack
+    return L;
+}
+
+struct BalWorkspace {
+    int32_t* counter;  // [S * H_kv] finished pieces per segment; zero between calls
+    float* piece_o;    // [W][2][G][D] normalised partial outputs, W = streaming warps
+    float* piece_ml;   // [W][2][G][2] (max, sum) in the log2 domain
+};
+
+__host__ __device__ inline size_t bal_align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+__host__ __device__ inline size_t bal_ws_bytes(int S, int Hkv, int G, int D, int W) {
+    return bal_align256(static_cast<size_t>(S) * Hkv * 4) + static_cast<size_t>(W) * 2 * G * D * 4 +
+           static_cast<size_t>(W) * 2 * G * 2 * 4;
+}
+
+__host__ __device__ inline BalWorkspace bal_ws(void* base, int S, int Hkv, int G, int D, int W) {
+    BalWorkspace w;
+    char* p = static_cast<char*>(base);
+    w.counter = reinterpret_cast<int32_t*>(p);
+    p += bal_align256(static_cast<size_t>(S) * Hkv * 4);
+    w.piece_o = reinterpret_cast<float*>(p);
+    p += static_cast<size_t>(W) * 2 * G * D * 4;
+    w.piece_ml = reinterpret_cast<float*>(p);
+    return w;
+}
+
+// First unit of slice c when U units are cut into C equal contiguous slices (one slice per
+// streaming warp).
+__host__ __device__ __forceinline__ int64_t slice_start(int64_t c, int64_t U, int64_t C) { return c * U / C; }
+// The slice that holds unit u (the last one among slices that start at or before u).
+__host__ __device__ __forceinline__ int64_t slice_owner(int64_t u, int64_t U, int64_t C) {
+    return ((u + 1) * C + U - 1) / U - 1;
+}
+
+// Sequence s with prefix[s] <= u < prefix[s + 1].
+__device__ __forceinline__ int32_t find_seq(const int32_t* prefix, int32_t S, int32_t u) {
+    int32_t lo = 0, hi = S;
+    while (hi - lo > 1) {
+        const int32_t mid = (lo + hi) >> 1;
+        if (prefix[mid] <= u) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+// Position in the work list: sequence s, kv head h, page j of np pages, sequence length len.
+struct Walker {
+    int32_t s, h, j, np, len;
+    __device__ __forceinline__ void at(const int32_t* prefix, const int32_t* lens, int32_t S, int32_t Hkv,
+                                       int32_t u) {
+        s = find_seq(prefix, S, u);
+        np = (prefix[s + 1] - prefix[s]) / Hkv;
+        const int32_t r = u - prefix[s];
+        h = r / np;
+        j = r - h * np;
+        len = lens[s];
+    }
+    __device__ __forceinline__ void advance(const int32_t* prefix, const int32_t* lens, int32_t S, int32_t Hkv) {
+        if (++j < np) return;
+        j = 0;
+        if (++h < Hkv) return;
+        h = 0;
+        do { ++s; } while (s < S && prefix[s + 1] == prefix[s]);
+        if (s < S) {
+            np = (prefix[s + 1] - prefix[s]) / Hkv;
+            len = lens[s];
+        }
+    }
+};
+
+__device__ __forceinline__ void bulk_copy_g2s(void* smem_dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(smem_dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Bounded wait that does not give up early on the abort flag (used to drain in-flight copies).
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > kWaitLimitNs) return;
+    }
+}
+
+// Merge of a segment's pieces by the warp that finished its last piece. Pieces are those of
+// the non-empty warp slices w_first..w_last (slot 1 for w_first when the segment starts
+// inside that slice). Heads go four at a time and pieces four at a time; lane l owns
+// head_dim elements E*l..E*l+E-1. Every load of a batch (the pieces' (m, l) and their
+// partial outputs) is issued before any is used, and a running maximum folds the batches:
+//   M' = max(M, m_j),  den = den 2^(M - M') + sum_j l_j 2^(m_j - M'),  acc likewise with o_j.
+template <int D>
+__device__ __forceinline__ void merge_pieces(__nv_bfloat16* o, int32_t a, int32_t w_first, int32_t w_last, int64_t U,
+                                             int64_t W, int32_t G, const BalWorkspace& ws, int32_t lane) {
+    constexpr int E = D / 32;
+    const bool may_be_empty = U < W;
+    const int32_t first_slot = slice_start(w_first, U, W) < a ? 1 : 0;
+    for (int32_t g0 = 0; g0 < G; g0 += 4) {
+        float M[4], den[4], acc[4][E];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            M[k] = -INFINITY;
+            den[k] = 0.f;
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[k][e] = 0.f;
+        }
+        for (int32_t w0 = w_first; w0 <= w_last; w0 += 4) {
+            float2 ml[4][4];
+            float v[4][4][E];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int32_t w = w0 + j;
+                bool ok = w <= w_last;
+                if (ok && may_be_empty) ok = slice_start(w, U, W) < slice_start(w + 1, U, W);
+                const int64_t piece = static_cast<int64_t>(w) * 2 + (w == w_first ? first_slot : 0);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    if (ok && g0 + k < G) {
+                        const int64_t pg = piece * G + g0 + k;
+                        ml[j][k] = __ldcg(reinterpret_cast<const float2*>(ws.piece_ml + pg * 2));
+                        const float* src = ws.piece_o + pg * D + lane * E;
+                        if constexpr (E == 4) {
+                            const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
+                            v[j][k][0] = t.x; v[j][k][1] = t.y; v[j][k][2] = t.z; v[j][k][3] = t.w;
+                        } else {
+                            const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
+                            v[j][k][0] = t.x; v[j][k][1] = t.y;
+                        }
+                    } else {
+                        ml[j][k] = make_float2(-INFINITY, 0.f);
+#pragma unroll
+                        for (int e = 0; e < E; ++e) v[j][k][e] = 0.f;
+                    }
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                float Mn = M[k];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) Mn = fmaxf(Mn, ml[j][k].x);
+                const float sc = (M[k] == -INFINITY) ? 0.f : exp2f(M[k] - Mn);
+                den[k] *= sc;
+#pragma unroll
+                for (int e = 0; e < E; ++e) acc[k][e] *= sc;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float wj = (ml[j][k].x == -INFINITY) ? 0.f : ml[j][k].y * exp2f(ml[j][k].x - Mn);
+                    den[k] += wj;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) acc[k][e] = fmaf(wj, v[j][k][e], acc[k][e]);
+                }
+                M[k] = Mn;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if (g0 + k < G) {
+                const float inv = 1.f / den[k];
+                uint32_t* dst = reinterpret_cast<uint32_t*>(o + (g0 + k) * D + lane * E);
+                dst[0] = pack_bf16x2(acc[k][0] * inv, acc[k][1] * inv);
+                if constexpr (E == 4) dst[1] = pack_bf16x2(acc[k][2] * inv, acc[k][3] * inv);
+            }
+        }
+    }
+}
+
+// Adds one finished piece to a segment's counter; acquire-release at device scope, so the
+// counting thread's warp saw its own piece stores (warp barrier before) and the last one to
+// count sees every other piece (warp barrier after, in the caller).
+__device__ __forceinline__ int32_t count_piece(int32_t* counter) {
+    int32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(counter) : "memory");
+    return old;
+}
+
+template <int D, int NW>
+__global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
+    const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+    __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ block_table,
+    int32_t max_blocks, const int32_t* __restrict__ seq_lens, int32_t S, int32_t num_kv_heads, int32_t G,
+    int32_t num_blocks, float scale_log2, int32_t nst, uint32_t stage_bytes, BalWorkspace ws, uint32_t* err) {
+    constexpr uint32_t kPage = kBlock * D * 2;
+    constexpr uint32_t kHalves = D / 64;
+    constexpr int KS = D / 16;  // k-steps over head_dim
+    constexpr int NT = D / 8;   // n-tiles of the output row
+    constexpr int NTH = NW * 32;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const BalLayout L = bal_layout(NW, nst, stage_bytes, S);
+    uint64_t* bars_all = reinterpret_cast<uint64_t*>(smem + L.bars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.flags);
+    int32_t* prefix = reinterpret_cast<int32_t*>(smem + L.prefix);
+    int32_t* lens = reinterpret_cast<int32_t*>(smem + L.lens);
+
+    const int32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int32_t cap = max_blocks * kBlock;
+    const int32_t Hq = G * num_kv_heads;
+
+    // Inputs may come from the kernel before this one in the stream (programmatic launch).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    // ---- prologue: clamped lengths and units per sequence, block-wide exclusive scan -------
+    {
+        const int32_t per = (S + NTH - 1) / NTH;
+        const int32_t b = min(S, tid * per), e = min(S, b + per);
+        int32_t local = 0;
+        for (int32_t s = b; s < e; ++s) {
+            int32_t len = __ldg(seq_lens + s);
+            if (len < 0 || len > cap) {
+                if (blockIdx.x == 0) raise_error(err, PA_DEVERR_LEN_RANGE);
+                len = len < 0 ? 0 : cap;
+            }
+            lens[s] = len;
+            local += ((len + kBlock - 1) / kBlock) * num_kv_heads;
+        }
+        int32_t incl = local;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int32_t v = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += v;
+        }
+        __shared__ int32_t warp_tot[NW];
+        if (lane == 31) warp_tot[warp] = incl;
+        if (lane == 0) {
+            for (int i = 0; i < nst; ++i) mbar_init(&bars_all[warp * nst + i], 1);
+        }
+        if (tid == 0) *abort_flag = 0;
+        fence_mbarrier_init();
+        __syncthreads();
+        int32_t base = 0;
+        for (int w = 0; w < warp; ++w) base += warp_tot[w];
+        int32_t run = base + incl - local;
+        for (int32_t s = b; s < e; ++s) {
+            prefix[s] = run;
+            run += ((lens[s] + kBlock - 1) / kBlock) * num_kv_heads;
+        }
+        if (tid == NTH - 1) prefix[S] = base + incl;
+        __syncthreads();
+    }
+    const int64_t U = prefix[S];
+    const int64_t W = static_cast<int64_t>(gridDim.x) * NW;  // streaming warps in the grid
+    // sequences without keys get zero rows (spread over the CTAs)
+    for (int32_t s = blockIdx.x; s < S; s += gridDim.x) {
+        if (lens[s] != 0) continue;
+        uint32_t* z = reinterpret_cast<uint32_t*>(out + static_cast<int64_t>(s) * Hq * D);
+        for (int32_t i = tid; i < Hq * D / 2; i += NTH) z[i] = 0u;
+    }
+    const int64_t gw = static_cast<int64_t>(blockIdx.x) * NW + warp;
+    const int32_t a_w = static_cast<int32_t>(slice_start(gw, U, W));
+    const int32_t b_w = static_cast<int32_t>(slice_start(gw + 1, U, W));
+    const int32_t n = b_w - a_w;
+    if (n <= 0) return;  // per warp: nothing below synchronises the CTA
+    uint8_t* ring = smem + L.ring + static_cast<uint32_t>(warp) * nst * stage_bytes;
+    const uint32_t ring_u32 = smem_u32(ring);
+    uint64_t* bars = bars_all + warp * nst;
+    const int32_t gid = lane >> 2, tig = lane & 3;
+
+    int32_t consumed = 0, issued = 0;
+    {
+        // Block-table row of unit a_w + 32 k + lane (pool row of its (block, kv head) page).
+        auto lane_row = [&](int32_t k) -> int32_t {
+            const int32_t u = a_w + 32 * k + lane;
+            if (u >= b_w) return 0;
+            const int32_t s = find_seq(prefix, S, u);
+            const int32_t np = (prefix[s + 1] - prefix[s]) / num_kv_heads;
+            const int32_t r = u - prefix[s];
+            const int32_t h = r / np, j = r - h * np;
+            int32_t phys = __ldg(block_table + static_cast<int64_t>(s) * max_blocks + j);
+            if (phys < 0 || phys >= num_blocks) {
+                raise_error(err, PA_DEVERR_BLOCK_RANGE);
+                phys = 0;
+            }
+            return (phys * num_kv_heads + h) * kBlock;
+        };
+        int32_t kc = 0;
+        int32_t id_cur = lane_row(0);
+        int32_t id_nxt = n > 32 ? lane_row(1) : 0;
+        Walker wi;
+        wi.at(prefix, lens, S, num_kv_heads, a_w);
+        // KV pages are read once per call: let them leave L2 first, ahead of the block table,
+        // queries, lengths and this kernel's own code.
+        const uint64_t kv_policy = l2_policy_evict_first();
+
+        auto issue = [&](int32_t t) {  // warp-uniform
+            if ((t >> 5) == kc + 1) {
+                ++kc;
+                id_cur = id_nxt;
+                id_nxt = 32 * (kc + 1) < n ? lane_row(kc + 1) : 0;
+            }
+            const int32_t row = __shfl_sync(0xffffffffu, id_cur, t & 31);
+            const bool seg_first = (t == 0) || (wi.j == 0);
+            if (lane == 0 && !*abort_flag) {
+                const int32_t st = t % nst;
+                uint8_t* stage = ring + static_cast<uint32_t>(st) * stage_bytes;
+                const uint32_t qbytes = static_cast<uint32_t>(G) * D * 2u;
+                mbar_arrive_expect_tx(&bars[st], 2u * kPage + (seg_first ? qbytes : 0u));
+#pragma unroll
+                for (uint32_t hf = 0; hf < kHalves; ++hf) {
+                    tma_load_2d_hint(stage + hf * 2048u, &tm_k, hf * 64, row, &bars[st], kv_policy);
+                    tma_load_2d_hint(stage + kPage + hf * 2048u, &tm_v, hf * 64, row, &bars[st], kv_policy);
+                }
+                if (seg_first) {
+                    bulk_copy_g2s(stage + 2u * kPage, q + (static_cast<int64_t>(wi.s) * Hq + wi.h * G) * D, qbytes,
+                                  &bars[st]);
+                }
+            }
+            wi.advance(prefix, lens, S, num_kv_heads);
+            issued = t + 1;
+        };
+
+        if (lane == 0) {
+            prefetch_tensormap(&tm_k);
+            prefetch_tensormap(&tm_v);
+        }
+        const int32_t pre = min(nst, n);
+        for (int32_t t = 0; t < pre; ++t) issue(t);
+
+        Walker wc;
+        wc.at(prefix, lens, S, num_kv_heads, a_w);
+        uint32_t qa[KS][4];
+        float acc[NT][4];
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+        int32_t t_first = 0;
+
+        for (int32_t t = 0; t < n; ++t) {
+            const int32_t st = t % nst;
+            const bool landed = mbar_wait_bounded(&bars[st], static_cast<uint32_t>(t / nst) & 1u, abort_flag);
+            if (!__all_sync(0xffffffffu, landed)) {  // lanes agree before any warp-wide step
+                if (lane == 0) {
+                    if (!*abort_flag) raise_error(err, PA_DEVERR_WAIT_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                __syncwarp();
+                break;
+            }
+            consumed = t + 1;
+            uint8_t* stage = ring + static_cast<uint32_t>(st) * stage_bytes;
+            const uint32_t k_u32 = ring_u32 + static_cast<uint32_t>(st) * stage_bytes;
+            const uint32_t v_u32 = k_u32 + kPage;
+            const bool seg_first = (t == 0) || (wc.j == 0);
+            if (seg_first) {
+                // the segment's G query rows were copied into this stage with the page
+                const __nv_bfloat16* qs = reinterpret_cast<const __nv_bfloat16*>(stage + 2u * kPage);
+                const bool r0 = gid < G, r1 = gid + 8 < G;
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks) {
+                    const int c0 = ks * 16 + tig * 2;
+                    qa[ks][0] = r0 ? *reinterpret_cast<const uint32_t*>(qs + gid * D + c0) : 0u;
+                    qa[ks][1] = r1 ? *reinterpret_cast<const uint32_t*>(qs + (gid + 8) * D + c0) : 0u;
+                    qa[ks][2] = r0 ? *reinterpret_cast<const uint32_t*>(qs + gid * D + c0 + 8) : 0u;
+                    qa[ks][3] = r1 ? *reinterpret_cast<const uint32_t*>(qs + (gid + 8) * D + c0 + 8) : 0u;
+                }
+#pragma unroll
+                for (int nn = 0; nn < NT; ++nn) acc[nn][0] = acc[nn][1] = acc[nn][2] = acc[nn][3] = 0.f;
+                m0 = m1 = -INFINITY;
+                l0 = l1 = 0.f;
+                t_first = t;
+            }
+            const int32_t ntok = min(kBlock, wc.len - wc.j * kBlock);
+            if (ntok < kBlock) {
+                // zero the V rows of the unused tail so that p = 0 contributes exactly nothing
+                const int32_t rows = kBlock - ntok;
+                for (int32_t c = lane; c < rows * 8 * static_cast<int32_t>(kHalves); c += 32) {
+                    const int32_t hf = c / (rows * 8), rem = c - hf * rows * 8;
+                    *reinterpret_cast<int4*>(stage + kPage + hf * 2048u + (ntok + rem / 8) * 128u + (rem % 8) * 16u) =
+                        make_int4(0, 0, 0, 0);
+                }
+                __syncwarp();
+            }
+
+            // S = Q K^T : rows = q heads (G of 16 valid), columns = the page's 16 tokens
+            float sc[2][4];
+#pragma unroll
+            for (int x = 0; x < 2; ++x) sc[x][0] = sc[x][1] = sc[x][2] = sc[x][3] = 0.f;
+            {
+                const uint32_t mat = lane >> 3, r = lane & 7;
+#pragma unroll
+                for (int p = 0; p < KS / 2; ++p) {
+#pragma unroll
+                    for (int x = 0; x < 2; ++x) {
+                        const uint32_t chunk = p * 4 + mat;
+                        const uint32_t addr = k_u32 + (chunk >> 3) * 2048u + sw128_offset(x * 8 + r, chunk & 7u);
+                        uint32_t b0, b1, b2, b3;
+                        ldsm_x4(addr, b0, b1, b2, b3);
+                        mma_16816(sc[x], qa[2 * p], b0, b1);
+                        mma_16816(sc[x], qa[2 * p + 1], b2, b3);
+                    }
+                }
+            }
+            // online softmax in the log2 domain; sc[x][e] is token 8x + 2 tig + (e & 1)
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int token = x * 8 + tig * 2 + (e & 1);
+                    const float v = token < ntok ? sc[x][e] * scale_log2 : -INFINITY;
+                    sc[x][e] = v;
+                    if (e < 2) mx0 = fmaxf(mx0, v); else mx1 = fmaxf(mx1, v);
+                }
+            }
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            const float c0 = exp2f(m0 - mn0), c1 = exp2f(m1 - mn1);
+            m0 = mn0;
+            m1 = mn1;
+            float ps[2][4];
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+                ps[x][0] = exp2f(sc[x][0] - mn0);
+                ps[x][1] = exp2f(sc[x][1] - mn0);
+                ps[x][2] = exp2f(sc[x][2] - mn1);
+                ps[x][3] = exp2f(sc[x][3] - mn1);
+            }
+            l0 = l0 * c0 + ps[0][0] + ps[0][1] + ps[1][0] + ps[1][1];
+            l1 = l1 * c1 + ps[0][2] + ps[0][3] + ps[1][2] + ps[1][3];
+#pragma unroll
+            for (int nn = 0; nn < NT; ++nn) {
+                acc[nn][0] *= c0;
+                acc[nn][1] *= c0;
+                acc[nn][2] *= c1;
+                acc[nn][3] *= c1;
+            }
+            uint32_t pa[4];
+            pa[0] = pack_bf16x2(ps[0][0], ps[0][1]);
+            pa[1] = pack_bf16x2(ps[0][2], ps[0][3]);
+            pa[2] = pack_bf16x2(ps[1][0], ps[1][1]);
+            pa[3] = pack_bf16x2(ps[1][2], ps[1][3]);
+            // O += P V
+            {
+                const uint32_t mat = lane >> 3, r = lane & 7;
+                const uint32_t token = (mat & 1u) * 8 + r;
+#pragma unroll
+                for (int p = 0; p < NT / 2; ++p) {
+                    const uint32_t chunk = p * 2 + (mat >> 1);
+                    const uint32_t addr = v_u32 + (chunk >> 3) * 2048u + sw128_offset(token, chunk & 7u);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_trans(addr, b0, b1, b2, b3);
+                    mma_16816(acc[2 * p], pa, b0, b1);
+                    mma_16816(acc[2 * p + 1], pa, b2, b3);
+                }
+            }
+
+            const bool seg_last = (t == n - 1) || (wc.j == wc.np - 1);
+            if (seg_last) {
+                float L0 = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
+                L0 += __shfl_xor_sync(0xffffffffu, L0, 2);
+                float L1 = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
+                L1 += __shfl_xor_sync(0xffffffffu, L1, 2);
+                const int32_t seg_a = prefix[wc.s] + wc.h * wc.np, seg_b = seg_a + wc.np;
+                const int32_t seg_id = wc.s * num_kv_heads + wc.h;
+                if (seg_a >= a_w && seg_b <= b_w) {
+                    // whole segment inside this warp: normalise and write out
+                    __nv_bfloat16* o = out + (static_cast<int64_t>(wc.s) * Hq + wc.h * G) * D;
+                    const float i0 = 1.f / L0, i1 = 1.f / L1;
+                    if (gid < G) {
+#pragma unroll
+                        for (int nn = 0; nn < NT; ++nn)
+                            *reinterpret_cast<uint32_t*>(o + gid * D + nn * 8 + tig * 2) =
+                                pack_bf16x2(acc[nn][0] * i0, acc[nn][1] * i0);
+                    }
+                    if (gid + 8 < G) {
+#pragma unroll
+                        for (int nn = 0; nn < NT; ++nn)
+                            *reinterpret_cast<uint32_t*>(o + (gid + 8) * D + nn * 8 + tig * 2) =
+                                pack_bf16x2(acc[nn][2] * i1, acc[nn][3] * i1);
+                    }
+                } else {
+                    // piece of a segment cut by the warp's slice: slot 0 = the slice's first
+                    // segment, slot 1 = its last one. The warp that adds the segment's last
+                    // piece merges them all and clears the counter for the next call.
+                    const int64_t piece = gw * 2 + ((t_first == 0) ? 0 : 1);
+                    float* po = ws.piece_o + piece * G * D;
+                    float* pml = ws.piece_ml + piece * G * 2;
+                    const float i0 = 1.f / L0, i1 = 1.f / L1;
+                    if (gid < G) {
+#pragma unroll
+                        for (int nn = 0; nn < NT; ++nn)
+                            *reinterpret_cast<float2*>(po + gid * D + nn * 8 + tig * 2) =
+                                make_float2(acc[nn][0] * i0, acc[nn][1] * i0);
+                        if (tig == 0) *reinterpret_cast<float2*>(pml + gid * 2) = make_float2(m0, L0);
+                    }
+                    if (gid + 8 < G) {
+#pragma unroll
+                        for (int nn = 0; nn < NT; ++nn)
+                            *reinterpret_cast<float2*>(po + (gid + 8) * D + nn * 8 + tig * 2) =
+                                make_float2(acc[nn][2] * i1, acc[nn][3] * i1);
+                        if (tig == 0) *reinterpret_cast<float2*>(pml + (gid + 8) * 2) = make_float2(m1, L1);
+                    }
+                    const int32_t w_first = static_cast<int32_t>(slice_owner(seg_a, U, W));
+                    const int32_t w_last = static_cast<int32_t>(slice_owner(seg_b - 1, U, W));
+                    const int32_t expected = (U >= W) ? (w_last - w_first + 1) : (seg_b - seg_a);
+                    __syncwarp();  // the warp's piece stores precede lane 0's release below
+                    int32_t last = 0;
+                    if (lane == 0) last = count_piece(ws.counter + seg_id) == expected - 1;
+                    last = __shfl_sync(0xffffffffu, last, 0);
+                    __syncwarp();  // lane 0's acquire precedes every lane's loads of other pieces
+                    if (last) {
+                        merge_pieces<D>(out + (static_cast<int64_t>(wc.s) * Hq + wc.h * G) * D, seg_a, w_first,
+                                        w_last, U, W, G, ws, lane);
+                        if (lane == 0) ws.counter[seg_id] = 0;
+                    }
+                }
+            }
+            __syncwarp();
+            if (ntok < kBlock) fence_proxy_async_shared();  // generic writes before the next copy
+            if (t + nst < n) issue(t + nst);
+            wc.advance(prefix, lens, S, num_kv_heads);
+        }
+        // after an abort: let the copies already issued land before the CTA can exit
+        if (consumed < issued && lane == 0) {
+            for (int32_t u = consumed; u < issued; ++u) mbar_drain(&bars[u % nst], static_cast<uint32_t>(u / nst) & 1u);
+        }
+    }
+}
+
+template <int D, int NW>
+cudaError_t launch_impl(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream) {
+    alignas(64) CUtensorMap tm_k, tm_v;
+    const uint64_t rows = static_cast<uint64_t>(a.num_blocks) * a.num_kv_heads * kBlock;
+    cudaError_t e = encode_bf16_2d_sw128(&tm_k, a.k_cache, D, rows, 64, kBlock);
+    if (e != cudaSuccess) return e;
+    e = encode_bf16_2d_sw128(&tm_v, a.v_cache, D, rows, 64, kBlock);
+    if (e != cudaSuccess) return e;
+    const int32_t G = a.num_q_heads / a.num_kv_heads;
+    e = cudaFuncSetAttribute(decode_balanced_kernel<D, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(plan.smem_bytes));
+    if (e != cudaSuccess) return e;
+    const int32_t W = plan.num_ctas * NW;
+    BalWorkspace ws = bal_ws(a.workspace, a.num_seqs, a.num_kv_heads, G, D, W);
+
+    // Programmatic launch: the grid may be scheduled while the previous kernel in the stream
+    // drains; it waits for that kernel (griddepcontrol.wait) before reading any input.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.num_ctas);
+    cfg.blockDim = dim3(NW * 32);
+    cfg.dynamicSmemBytes = plan.smem_bytes;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_balanced_kernel<D, NW>, tm_k, tm_v, static_cast<__nv_bfloat16*>(a.out),
+                              static_cast<const __nv_bfloat16*>(a.q), a.block_table, a.max_blocks_per_seq,
+                              a.seq_lens, a.num_seqs, a.num_kv_heads, G, a.num_blocks, a.scale * kLog2e, plan.stages,
+                              plan.stage_bytes, ws, a.err);
+}
+
+template <int D, int NW>
+int ctas_per_sm(uint32_t smem) {
+    int n = 0;
+    if (cudaFuncSetAttribute(decode_balanced_kernel<D, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+        return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_balanced_kernel<D, NW>, NW * 32, smem) !=
+        cudaSuccess)
+        return 0;
+    return n;
+}
+
+}  // namespace
+
+bool plan_decode_balanced(int32_t S, int32_t Hkv, int32_t G, int32_t D, const DeviceInfo& dev, DecodePlan* plan) {
+    if (G < 4 || G > kBalMaxGroup || (D != 64 && D != 128) || S > kBalMaxSeqs || S < 1) return false;
+    const uint32_t stage = bal_stage_bytes(D, G);
+    // Prefer 8 warps per CTA with 2..4 stages each; fall back to 4 warps for large groups.
+    for (int NW : {8, 4}) {
+        for (int nst = 4; nst >= 2; --nst) {
+            const BalLayout L = bal_layout(NW, nst, stage, S);
+            if (L.total > static_cast<uint32_t>(dev.max_smem_optin)) continue;
+            const int per_sm = (D == 128) ? (NW == 8 ? ctas_per_sm<128, 8>(L.total) : ctas_per_sm<128, 4>(L.total))
+                                          : (NW == 8 ? ctas_per_sm<64, 8>(L.total) : ctas_per_sm<64, 4>(L.total));
+            if (per_sm < 1) continue;
+            const int ctas = dev.num_sms * per_sm;
+            if (ctas * NW > kBalMaxWarps) continue;
+            plan->path = kDecodeMmaBalanced;
+            plan->warps = NW;
+            plan->stages = nst;
+            plan->stage_bytes = stage;
+            plan->smem_bytes = L.total;
+            plan->num_ctas = ctas;
+            plan->workspace_bytes = bal_ws_bytes(S, Hkv, G, D, ctas * NW);
+            return true;
+        }
+    }
+    return false;
+}
+
+cudaError_t launch_decode_balanced(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream) {
+    if (a.head_dim == 128)
+        return plan.warps == 8 ? launch_impl<128, 8>(a, plan, stream) : launch_impl<128, 4>(a, plan, stream);
+    return plan.warps == 8 ? launch_impl<64, 8>(a, plan, stream) : launch_impl<64, 4>(a, plan, stream);
+}
+
+}  // namespace pa

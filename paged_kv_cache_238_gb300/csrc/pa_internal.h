@@ -1,0 +1,122 @@
+// Internal host-side interface between the C ABI (pa_api.cu) and the kernel translation
+// units. Not installed; not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/pa.h"
+
+namespace pa {
+
+// ------------------------------------------------------------------------------------------
+// reshape_and_cache
+// ------------------------------------------------------------------------------------------
+struct ReshapeArgs {
+    const void* k;
+    const void* v;
+    void* k_cache;
+    void* v_cache;
+    const int64_t* slot_mapping;
+    int32_t num_tokens, num_kv_heads, head_dim, num_blocks;
+    int32_t elem_bytes;
+    uint32_t* err;
+};
+cudaError_t launch_reshape_and_cache(const ReshapeArgs& a, int num_sms, cudaStream_t stream);
+
+// ------------------------------------------------------------------------------------------
+// decode
+// ------------------------------------------------------------------------------------------
+struct DecodeArgs {
+    void* out;
+    const void* q;
+    const void* k_cache;
+    const void* v_cache;
+    const int32_t* block_table;
+    int32_t max_blocks_per_seq;
+    const int32_t* seq_lens;
+    int32_t num_seqs, max_seq_len, num_q_heads, num_kv_heads, head_dim, num_blocks;
+    float scale;
+    pa_dtype dtype;
+    void* workspace;
+    size_t workspace_bytes;
+    uint32_t* err;
+};
+
+enum DecodePath : int {
+    kDecodeSimtSplit = 0,   // CUDA-core kernel over (sequence, kv head, partition) + reduce
+    kDecodeMmaBalanced = 1  // persistent TMA + mma.sync kernel over a balanced page list + reduce
+};
+
+struct DecodePlan {
+    DecodePath path;
+    int32_t partition_tokens;  // simt: tokens per partition (multiple of 16)
+    int32_t num_partitions;    // simt: ceil(max_seq_len / partition_tokens)
+    int32_t head_chunks;       // simt: q heads are processed in chunks of up to 4
+    int32_t num_ctas;          // balanced: persistent grid size
+    int32_t warps;             // balanced: independent streaming warps per CTA
+    int32_t stages;            // balanced: ring stages per warp
+    uint32_t stage_bytes;      // balanced: bytes per stage (K page, V page, query rows)
+    uint32_t smem_bytes;       // balanced: dynamic shared memory per CTA
+    size_t workspace_bytes;
+};
+
+struct DeviceInfo {
+    int device;
+    int num_sms;
+    int max_smem_optin;
+};
+
+// Fills `info` for the current device (cached per device after the first call).
+cudaError_t current_device_info(DeviceInfo* info);
+
+DecodePlan plan_decode(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                       int32_t max_seq_len, pa_dtype dtype, const DeviceInfo& dev);
+cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream);
+
+// Balanced bf16 path (decode_balanced.cu): fills `plan` and returns true when the shape is
+// eligible (GQA group 4..16, head_dim 64/128, at most 1024 sequences) and fits the device.
+bool plan_decode_balanced(int32_t num_seqs, int32_t num_kv_heads, int32_t group, int32_t head_dim,
+                          const DeviceInfo& dev, DecodePlan* plan);
+cudaError_t launch_decode_balanced(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream);
+
+// SIMT path (decode_simt.cu).
+cudaError_t launch_decode_simt(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream);
+int simt_heads_per_cta();
+
+// ------------------------------------------------------------------------------------------
+// prefill
+// ------------------------------------------------------------------------------------------
+struct PrefillArgs {
+    void* out;
+    const void* q;
+    const void* k_cache;
+    const void* v_cache;
+    const int32_t* block_table;
+    int32_t max_blocks_per_seq;
+    const int32_t* seq_lens;
+    const int32_t* query_start_loc;
+    int32_t num_seqs, max_chunk_len, max_seq_len, num_q_heads, num_kv_heads, head_dim, num_blocks;
+    float scale;
+    pa_dtype dtype;
+    uint32_t* err;
+};
+// total_rows: number of chunk rows (query_start_loc[num_seqs]); the host cannot read it, so
+// the caller passes an upper bound (grid rows past the end exit at once).
+cudaError_t launch_prefill(const PrefillArgs& a, const DeviceInfo& dev, cudaStream_t stream);
+// General CUDA-core path (any dtype / head_dim 64/128): one CTA per chunk row and head chunk.
+cudaError_t launch_prefill_simt(const PrefillArgs& a, int32_t total_rows, cudaStream_t stream);
+
+// ------------------------------------------------------------------------------------------
+// tensor maps (driver entry point resolved at run time; no libcuda link needed)
+// ------------------------------------------------------------------------------------------
+// Encodes a 2-D bf16 tensor map over `rows` rows of `cols` elements (row pitch cols*2 bytes)
+// with a box of box_cols x box_rows and 128-byte swizzle. `map` must point to 128 bytes.
+cudaError_t encode_bf16_2d_sw128(void* map, const void* base, uint64_t cols, uint64_t rows,
+                                 uint32_t box_cols, uint32_t box_rows);
+// 3-D variant: dims (innermost first) d0 x d1 x d2 with byte strides s1 (dim 1) and s2 (dim 2).
+cudaError_t encode_bf16_3d_sw128(void* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                                 uint64_t s1_bytes, uint64_t s2_bytes, uint32_t b0, uint32_t b1, uint32_t b2);
+
+}  // namespace pa

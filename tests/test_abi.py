@@ -1,0 +1,134 @@
+"""CPU-only checks of the C ABI: the library builds, loads and exports every symbol that
+include/pa.h declares, and host-checkable argument errors are rejected before any CUDA call
+(no compute runs here)."""
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+from paged_kv_cache_238_gb300 import binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+pytestmark = pytest.mark.skipif(shutil.which("nvcc") is None and not os.path.exists(
+    os.path.join(ROOT, "paged_kv_cache_238_gb300", "libpa.so")), reason="needs nvcc to build libpa")
+
+FAKE = 0x10000  # a 16-byte-aligned non-null address; never dereferenced by these calls
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "pa.h")).read()
+    return sorted(set(re.findall(r"PA_API\s+[\w\s\*]+?\b(pa_\w+)\s*\(", text)))
+
+
+def test_header_and_binding_agree():
+    assert declared_symbols() == sorted(B.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = B.load()
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings():
+    assert B.status_string(B.PA_OK) == "PA_OK"
+    assert B.status_string(B.PA_ERR_INVALID_ARG) == "PA_ERR_INVALID_ARG"
+    assert B.status_string(B.PA_ERR_UNSUPPORTED) == "PA_ERR_UNSUPPORTED"
+    assert B.status_string(B.PA_ERR_CUDA) == "PA_ERR_CUDA"
+    assert B.status_string(99) == "PA_UNKNOWN_STATUS"
+
+
+def _decode(lib, **kw):
+    args = dict(out=FAKE, q=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, mb=4, lens=FAKE, S=2, max_len=64, Hq=8, Hkv=2,
+                D=128, NB=16, scale=0.1, dt=B.PA_BF16, ws=FAKE, ws_bytes=1 << 20, stream=None)
+    args.update(kw)
+    return lib.pa_decode(args["out"], args["q"], args["kc"], args["vc"], args["bt"], args["mb"], args["lens"],
+                         args["S"], args["max_len"], args["Hq"], args["Hkv"], args["D"], args["NB"], args["scale"],
+                         args["dt"], args["ws"], args["ws_bytes"], args["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(Hq=6, Hkv=4), B.PA_ERR_INVALID_ARG),           # q heads not a multiple of kv heads
+    (dict(Hkv=0), B.PA_ERR_INVALID_ARG),
+    (dict(D=96), B.PA_ERR_UNSUPPORTED),                    # head_dim outside {64, 128}
+    (dict(D=0), B.PA_ERR_INVALID_ARG),
+    (dict(dt=7), B.PA_ERR_INVALID_ARG),
+    (dict(q=None), B.PA_ERR_INVALID_ARG),
+    (dict(bt=None), B.PA_ERR_INVALID_ARG),
+    (dict(out=FAKE + 8), B.PA_ERR_INVALID_ARG),            # misaligned
+    (dict(lens=FAKE + 2), B.PA_ERR_INVALID_ARG),           # misaligned int32 array
+    (dict(max_len=65), B.PA_ERR_INVALID_ARG),              # beyond max_blocks * 16
+    (dict(S=-1), B.PA_ERR_INVALID_ARG),
+    (dict(NB=0), B.PA_ERR_INVALID_ARG),
+    (dict(NB=1 << 27, Hkv=2), B.PA_ERR_UNSUPPORTED),       # pool rows beyond 32-bit coordinates
+])
+def test_decode_rejects_bad_arguments(kw, expect):
+    assert _decode(B.load(), **kw) == expect
+
+
+def test_decode_zero_sequences_is_a_no_op():
+    assert _decode(B.load(), S=0, out=None, q=None) == B.PA_OK
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(T=-1), B.PA_ERR_INVALID_ARG),
+    (dict(H=0), B.PA_ERR_INVALID_ARG),
+    (dict(D=12), B.PA_ERR_UNSUPPORTED),                    # row not a multiple of 16 bytes (bf16)
+    (dict(slots=None), B.PA_ERR_INVALID_ARG),
+    (dict(slots=FAKE + 4), B.PA_ERR_INVALID_ARG),
+    (dict(k=FAKE + 2), B.PA_ERR_INVALID_ARG),
+    (dict(dt=5), B.PA_ERR_INVALID_ARG),
+    (dict(T=0, k=None), B.PA_OK),                          # nothing to write
+])
+def test_reshape_rejects_bad_arguments(kw, expect):
+    a = dict(k=FAKE, v=FAKE, kc=FAKE, vc=FAKE, slots=FAKE, T=4, H=2, D=128, NB=8, dt=B.PA_BF16)
+    a.update(kw)
+    assert B.load().pa_reshape_and_cache(a["k"], a["v"], a["kc"], a["vc"], a["slots"], a["T"], a["H"], a["D"],
+                                         a["NB"], a["dt"], None) == expect
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(max_chunk=65), B.PA_ERR_INVALID_ARG),            # chunk longer than any sequence may be
+    (dict(qsl=None), B.PA_ERR_INVALID_ARG),
+    (dict(max_chunk=-1), B.PA_ERR_INVALID_ARG),
+    (dict(D=80), B.PA_ERR_UNSUPPORTED),
+    (dict(max_chunk=0, q=None), B.PA_OK),
+])
+def test_prefill_rejects_bad_arguments(kw, expect):
+    a = dict(out=FAKE, q=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, mb=4, lens=FAKE, qsl=FAKE, S=2, max_chunk=16,
+             max_len=64, Hq=8, Hkv=2, D=128, NB=16, dt=B.PA_BF16)
+    a.update(kw)
+    assert B.load().pa_prefill_chunk(a["out"], a["q"], a["kc"], a["vc"], a["bt"], a["mb"], a["lens"], a["qsl"],
+                                     a["S"], a["max_chunk"], a["max_len"], a["Hq"], a["Hkv"], a["D"], a["NB"],
+                                     0.1, a["dt"], None) == expect
+
+
+def test_workspace_size_of_invalid_shape_is_zero():
+    assert B.load().pa_decode_workspace_size(2, 6, 4, 128, 64, B.PA_BF16) == 0
+
+
+def test_device_errors_needs_an_output_pointer():
+    assert B.load().pa_get_device_errors(None, 0) == B.PA_ERR_INVALID_ARG
+
+
+def test_product_path_does_not_reference_the_oracle():
+    """The CUDA library and its binding never load, link or import the oracle."""
+    pkg = os.path.join(ROOT, "paged_kv_cache_238_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "liboracle" not in text and "pa_oracle" not in text, f
+    with open(os.path.join(ROOT, "include", "pa.h")) as fh:
+        assert "oracle" not in fh.read()
+
+
+def test_library_does_not_link_the_oracle():
+    lib = B.load()
+    for sym in ("oracle_attention", "oracle_reshape_and_cache"):
+        with pytest.raises(AttributeError):
+            getattr(lib, sym)
+    assert isinstance(lib, ctypes.CDLL)
