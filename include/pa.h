@@ -167,6 +167,34 @@ PA_API pa_status pa_prefill_chunk(void* out, const void* q, const void* k_cache,
                            int32_t num_blocks, float scale, pa_dtype dtype, void* stream);
 
 /*
+ * pa_decode_noalloc: pa_decode for callers that cannot allocate device memory. The source
+ * pages have no counterpart for this entry point; it exists for callers such as a host
+ * framework that owns the whole device-memory budget and lets no plug-in allocate, a plug-in
+ * that only receives tensors and has no allocator, or a latency-critical path that must not
+ * call cudaMalloc/cudaFree (they can synchronise the device).
+ *
+ * Same arguments and results as pa_decode, without the workspace: the split-KV scratch lives
+ * in a fixed array of PA_DECODE_NOALLOC_MAX_BYTES that the library holds in device memory on
+ * every GPU that loads it, until the process exits. The call allocates nothing (no
+ * cudaMalloc, cudaFree or allocating library routine).
+ *   - Shapes whose pa_decode_workspace_size exceeds PA_DECODE_NOALLOC_MAX_BYTES are rejected
+ *     with PA_ERR_UNSUPPORTED before anything is launched.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ *     with that device current; make that first call before any stream capture.
+ *   - Every call shares the one array, which keeps what the previous call left; the call
+ *     itself clears the part that must start at zero (an asynchronous memset on `stream`).
+ *     Calls that overlap on the GPU (different streams, or concurrent graphs) race on the
+ *     array and give wrong results: serialise them.
+ */
+#define PA_DECODE_NOALLOC_MAX_BYTES (16u * 1024u * 1024u)
+
+PA_API pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* block_table, int32_t max_blocks_per_seq,
+                                   const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                   int32_t num_blocks, float scale, pa_dtype dtype, void* stream);
+
+/*
  * pa_get_device_errors: read the device error word of the current device (PA_DEVERR_*
  * bits OR-ed by the kernels since the last clear) into *errors, and clear it when
  * `clear` is non-zero. Synchronises the current device. The library owns the word.

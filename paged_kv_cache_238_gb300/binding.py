@@ -20,7 +20,9 @@ BLOCK_SIZE = 16
 
 #: every symbol that include/pa.h declares
 EXPORTED = ("pa_reshape_and_cache", "pa_decode_workspace_size", "pa_decode", "pa_prefill_chunk",
-            "pa_get_device_errors", "pa_status_string")
+            "pa_decode_noalloc", "pa_get_device_errors", "pa_status_string")
+#: size of the library's fixed scratch used by pa_decode_noalloc
+PA_DECODE_NOALLOC_MAX_BYTES = 16 * 1024 * 1024
 
 _lock = threading.Lock()
 _lib = None
@@ -52,6 +54,9 @@ def load(build_if_needed: bool = True) -> ctypes.CDLL:
             lib.pa_prefill_chunk.restype = ctypes.c_int
             lib.pa_prefill_chunk.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32,
                                              i32, f32, ctypes.c_int, vp]
+            lib.pa_decode_noalloc.restype = ctypes.c_int
+            lib.pa_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, f32,
+                                              ctypes.c_int, vp]
             lib.pa_get_device_errors.restype = ctypes.c_int
             lib.pa_get_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
             _lib = lib
@@ -125,6 +130,19 @@ def pa_decode(out, q, k_cache, v_cache, block_table, seq_lens, max_seq_len: int,
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
         _ptr(seq_lens), S, int(max_seq_len), H_q, H_kv, D, NB, float(scale), _dtype_code(q), _ptr(workspace),
         ws_bytes, _stream(stream)))
+
+
+def pa_decode_noalloc(out, q, k_cache, v_cache, block_table, seq_lens, max_seq_len: int, scale: float,
+                      stream=None) -> None:
+    """pa_decode without a workspace argument, for callers that cannot allocate device
+    memory: the library's fixed device scratch (PA_DECODE_NOALLOC_MAX_BYTES) is used instead.
+    Calls share that scratch, so they must not overlap on the GPU."""
+    _need_cuda(out, q, k_cache, v_cache, block_table, seq_lens)
+    S, H_q, D = q.shape
+    NB, H_kv = k_cache.shape[0], k_cache.shape[1]
+    _check("pa_decode_noalloc", load().pa_decode_noalloc(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
+        _ptr(seq_lens), S, int(max_seq_len), H_q, H_kv, D, NB, float(scale), _dtype_code(q), _stream(stream)))
 
 
 def pa_prefill_chunk(out, q, k_cache, v_cache, block_table, seq_lens, query_start_loc, max_chunk_len: int,
