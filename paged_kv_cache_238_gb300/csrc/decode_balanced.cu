@@ -1,30 +1,33 @@
-// Balanced persistent decode kernel for bf16 GQA groups of 4..16 q heads per kv head
-// (TMA page staging + mma.sync), and its split reduce.
+// Balanced persistent decode kernel for bf16 GQA groups of 4..16 q heads per kv head:
+// TMA page staging, mma.sync, and a split-KV reduce done in place.
 //
 // Work list. The unit of work is one (sequence, kv head, logical block) page: 16 tokens x
 // head_dim of K plus the same of V (8 KB at head_dim 128). Units are ordered sequence-major,
 // then kv head, then page, so the units of one (sequence, kv head) "segment" are contiguous.
-// Every CTA rebuilds the same list from seq_lens with a block-wide scan and takes an equal
-// contiguous slice; inside the CTA every warp takes an equal contiguous sub-slice. The grid
-// is one wave of persistent CTAs, and per-SM work differs by at most one page whatever the
-// mix of lengths.
+// Every CTA rebuilds the list's prefix sums from seq_lens with a block-wide scan and takes an
+// equal contiguous slice of it (one persistent CTA per SM); inside the CTA each warp takes an
+// equal contiguous sub-slice. Per-SM work differs by at most one page whatever the mix of
+// lengths.
 //
 // Streaming. Each warp is an independent worker with its own ring of stages in shared memory.
-// Lane 0 resolves the page's physical block through the block table ("My Understanding of
-// vLLM and PagedAttention", "Block Table"), then issues two 2-D TMA tile copies per 64-column
-// half (K and V, 128-byte swizzle) completing on the stage's mbarrier; when the unit starts a
-// new segment it also bulk-copies that segment's G query rows into the stage. Block ids are
-// fetched 32 units ahead by the warp's lanes. The warp consumes a stage (S = Q K^T and O += P V
-// on mma.sync m16n8k16, rows = the G q heads that share the kv head, so each page is read once
-// for the whole group; online softmax in registers, log2 domain) and refills it with the
-// unit `stages` ahead. The unused tail of a sequence's last block may hold anything: its keys
-// are masked to -inf and its V rows are zeroed in shared memory before P V.
+// Lane 0 resolves a page's physical block through the block table ("My Understanding of vLLM
+// and PagedAttention", "Block Table") and issues the page's K and V as 2-D TMA tile copies
+// (128-byte swizzle, 64-column boxes) completing on the stage's mbarrier; when the unit starts
+// a new segment it also bulk-copies that segment's G query rows into the stage. Block ids are
+// fetched 32 units ahead by the warp's lanes. The warp consumes a stage (S = Q K^T and
+// O += P V on mma.sync m16n8k16 with the G q heads that share a kv head as rows, so each page
+// is read once for the whole group; online softmax in registers, log2 domain) and refills it
+// with the unit `stages` ahead. The unused tail of a sequence's last block may hold anything:
+// its keys are masked to -inf and its V rows zeroed in shared memory before P V.
 //
-// Merging. A segment that lies wholly inside a warp's sub-slice is normalised and written
-// from registers. Pieces of segments cut by sub-slice boundaries meet in shared memory after
-// one CTA barrier; segments cut by CTA boundaries leave (m, l, o) pieces in the workspace, and
-// the reduce kernel (launched with programmatic dependent launch, so its launch overlaps the
-// main kernel) merges them:  M = max m_p, w_p = l_p 2^(m_p - M), out = sum w_p o_p / sum w_p.
+// Split-KV reduce, in three levels, all with the same log-sum-exp merge
+//   M = max_p m_p,  w_p = l_p 2^(m_p - M),  out = sum_p w_p o_p / sum_p w_p :
+//  1. a segment inside one warp's sub-slice is normalised and written from registers;
+//  2. pieces cut by warp boundaries meet in shared memory after one CTA barrier and are
+//     merged there by the warp at which the segment's run of pieces starts;
+//  3. segments cut by CTA boundaries leave one piece per CTA in the workspace; the warp that
+//     counts the last piece (device-scope acquire-release counter per segment) merges them
+//     and puts the counter back to zero.
 #include <cuda.h>  // CUtensorMap (type only)
 #include <math.h>
 
@@ -36,8 +39,7 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kBalMaxGroup = 16;
-constexpr int kBalMaxSeqs = 1024;     // per-sequence tables live in shared memory
-constexpr int kBalMaxWarps = 2048;    // streaming warps in the grid (bounds the piece list)
+constexpr int kBalMaxSeqs = 1024;  // per-sequence tables live in shared memory
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
@@ -47,47 +49,49 @@ __host__ __device__ inline uint32_t bal_stage_bytes(int D, int G) {
 }
 
 struct BalLayout {
-    uint32_t ring, bars, flags, prefix, lens, total;
+    uint32_t ring, piece0, piece_ml, meta, bars, flags, prefix, lens, total;
 };
 
-__host__ __device__ inline BalLayout bal_layout(int NW, int nst, uint32_t stage_bytes, int S) {
+__host__ __device__ inline BalLayout bal_layout(int NW, int nst, uint32_t stage_bytes, int G, int D, int S) {
     BalLayout L;
     uint32_t o = 0;
-    L.ring = o;    o += static_cast<uint32_t>(NW) * nst * stage_bytes;
-    L.bars = o;    o += static_cast<uint32_t>(NW) * nst * 8u;
-    L.flags = o;   o += 16u;
-    L.prefix = o;  o += align_up((S + 1) * 4u, 16u);
-    L.lens = o;    o += align_up(S * 4u, 16u);
+    L.ring = o;      o += static_cast<uint32_t>(NW) * nst * stage_bytes;
+    L.piece0 = o;    o += static_cast<uint32_t>(NW) * G * D * 4u;             // each warp's first piece
+    L.piece_ml = o;  o += static_cast<uint32_t>(NW) * 2u * G * 2u * 4u;       // (m, l) of both pieces
+    L.meta = o;      o += align_up(static_cast<uint32_t>(NW) * 2u * 4u, 16u);  // segment of each piece
+    L.bars = o;      o += static_cast<uint32_t>(NW) * nst * 8u;
+    L.flags = o;     o += 16u;
+    L.prefix = o;    o += align_up((S + 1) * 4u, 16u);
+    L.lens = o;      o += align_up(S * 4u, 16u);
     L.total = o + 1024u;  // base alignment slack
     return L;
 }
 
 struct BalWorkspace {
-    int32_t* counter;  // [S * H_kv] finished pieces per segment; zero between calls
-    float* piece_o;    // [W][2][G][D] normalised partial outputs, W = streaming warps
-    float* piece_ml;   // [W][2][G][2] (max, sum) in the log2 domain
+    int32_t* counter;  // [S * H_kv] finished CTA pieces per segment; zero between calls
+    float* piece_o;    // [C][2][G][D] normalised partial outputs of CTA pieces
+    float* piece_ml;   // [C][2][G][2] (max, sum) in the log2 domain
 };
 
 __host__ __device__ inline size_t bal_align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-__host__ __device__ inline size_t bal_ws_bytes(int S, int Hkv, int G, int D, int W) {
-    return bal_align256(static_cast<size_t>(S) * Hkv * 4) + static_cast<size_t>(W) * 2 * G * D * 4 +
-           static_cast<size_t>(W) * 2 * G * 2 * 4;
+__host__ __device__ inline size_t bal_ws_bytes(int S, int Hkv, int G, int D, int C) {
+    return bal_align256(static_cast<size_t>(S) * Hkv * 4) + static_cast<size_t>(C) * 2 * G * D * 4 +
+           static_cast<size_t>(C) * 2 * G * 2 * 4;
 }
 
-__host__ __device__ inline BalWorkspace bal_ws(void* base, int S, int Hkv, int G, int D, int W) {
+__host__ __device__ inline BalWorkspace bal_ws(void* base, int S, int Hkv, int G, int D, int C) {
     BalWorkspace w;
     char* p = static_cast<char*>(base);
     w.counter = reinterpret_cast<int32_t*>(p);
     p += bal_align256(static_cast<size_t>(S) * Hkv * 4);
     w.piece_o = reinterpret_cast<float*>(p);
-    p += static_cast<size_t>(W) * 2 * G * D * 4;
+    p += static_cast<size_t>(C) * 2 * G * D * 4;
     w.piece_ml = reinterpret_cast<float*>(p);
     return w;
 }
 
-// First unit of slice c when U units are cut into C equal contiguous slices (one slice per
-// streaming warp).
+// First unit of slice c when U units are cut into C equal contiguous slices.
 __host__ __device__ __forceinline__ int64_t slice_start(int64_t c, int64_t U, int64_t C) { return c * U / C; }
 // The slice that holds unit u (the last one among slices that start at or before u).
 __host__ __device__ __forceinline__ int64_t slice_owner(int64_t u, int64_t U, int64_t C) {
@@ -145,8 +149,8 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
     }
 }
 
-// Merge of a segment's pieces by the warp that finished its last piece. Pieces are those of
-// the non-empty warp slices w_first..w_last (slot 1 for w_first when the segment starts
+// Merge of a segment's CTA pieces by the warp that counted its last one. Pieces are those of
+// the non-empty CTA slices w_first..w_last of W (slot 1 for w_first when the segment starts
 // inside that slice). Heads go four at a time and pieces four at a time; lane l owns
 // head_dim elements E*l..E*l+E-1. Every load of a batch (the pieces' (m, l) and their
 // partial outputs) is issued before any is used, and a running maximum folds the batches:
@@ -245,10 +249,14 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
     constexpr uint32_t kHalves = D / 64;
     constexpr int KS = D / 16;  // k-steps over head_dim
     constexpr int NT = D / 8;   // n-tiles of the output row
+    constexpr int E = D / 32;   // elements per lane in the merges
     constexpr int NTH = NW * 32;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const BalLayout L = bal_layout(NW, nst, stage_bytes, S);
+    const BalLayout L = bal_layout(NW, nst, stage_bytes, G, D, S);
+    float* piece0 = reinterpret_cast<float*>(smem + L.piece0);
+    float* piece_ml = reinterpret_cast<float*>(smem + L.piece_ml);
+    int32_t* meta = reinterpret_cast<int32_t*>(smem + L.meta);
     uint64_t* bars_all = reinterpret_cast<uint64_t*>(smem + L.bars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.flags);
     int32_t* prefix = reinterpret_cast<int32_t*>(smem + L.prefix);
@@ -284,6 +292,8 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
         __shared__ int32_t warp_tot[NW];
         if (lane == 31) warp_tot[warp] = incl;
         if (lane == 0) {
+            meta[warp * 2] = -1;
+            meta[warp * 2 + 1] = -1;
             for (int i = 0; i < nst; ++i) mbar_init(&bars_all[warp * nst + i], 1);
         }
         if (tid == 0) *abort_flag = 0;
@@ -299,26 +309,29 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
         if (tid == NTH - 1) prefix[S] = base + incl;
         __syncthreads();
     }
+
     const int64_t U = prefix[S];
-    const int64_t W = static_cast<int64_t>(gridDim.x) * NW;  // streaming warps in the grid
+    const int64_t C = gridDim.x;
     // sequences without keys get zero rows (spread over the CTAs)
     for (int32_t s = blockIdx.x; s < S; s += gridDim.x) {
         if (lens[s] != 0) continue;
         uint32_t* z = reinterpret_cast<uint32_t*>(out + static_cast<int64_t>(s) * Hq * D);
         for (int32_t i = tid; i < Hq * D / 2; i += NTH) z[i] = 0u;
     }
-    const int64_t gw = static_cast<int64_t>(blockIdx.x) * NW + warp;
-    const int32_t a_w = static_cast<int32_t>(slice_start(gw, U, W));
-    const int32_t b_w = static_cast<int32_t>(slice_start(gw + 1, U, W));
+    const int32_t u0 = static_cast<int32_t>(slice_start(blockIdx.x, U, C));
+    const int32_t u1 = static_cast<int32_t>(slice_start(blockIdx.x + 1, U, C));
+    if (u0 >= u1) return;  // uniform over the CTA
+    const int32_t n_cta = u1 - u0;
+    const int32_t a_w = u0 + static_cast<int32_t>((static_cast<int64_t>(warp) * n_cta) / NW);
+    const int32_t b_w = u0 + static_cast<int32_t>((static_cast<int64_t>(warp + 1) * n_cta) / NW);
     const int32_t n = b_w - a_w;
-    if (n <= 0) return;  // per warp: nothing below synchronises the CTA
     uint8_t* ring = smem + L.ring + static_cast<uint32_t>(warp) * nst * stage_bytes;
     const uint32_t ring_u32 = smem_u32(ring);
     uint64_t* bars = bars_all + warp * nst;
     const int32_t gid = lane >> 2, tig = lane & 3;
 
     int32_t consumed = 0, issued = 0;
-    {
+    if (n > 0) {
         // Block-table row of unit a_w + 32 k + lane (pool row of its (block, kv head) page).
         auto lane_row = [&](int32_t k) -> int32_t {
             const int32_t u = a_w + 32 * k + lane;
@@ -513,7 +526,6 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
                 float L1 = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
                 L1 += __shfl_xor_sync(0xffffffffu, L1, 2);
                 const int32_t seg_a = prefix[wc.s] + wc.h * wc.np, seg_b = seg_a + wc.np;
-                const int32_t seg_id = wc.s * num_kv_heads + wc.h;
                 if (seg_a >= a_w && seg_b <= b_w) {
                     // whole segment inside this warp: normalise and write out
                     __nv_bfloat16* o = out + (static_cast<int64_t>(wc.s) * Hq + wc.h * G) * D;
@@ -531,40 +543,32 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
                                 pack_bf16x2(acc[nn][2] * i1, acc[nn][3] * i1);
                     }
                 } else {
-                    // piece of a segment cut by the warp's slice: slot 0 = the slice's first
-                    // segment, slot 1 = its last one. The warp that adds the segment's last
-                    // piece merges them all and clears the counter for the next call.
-                    const int64_t piece = gw * 2 + ((t_first == 0) ? 0 : 1);
-                    float* po = ws.piece_o + piece * G * D;
-                    float* pml = ws.piece_ml + piece * G * 2;
-                    const float i0 = 1.f / L0, i1 = 1.f / L1;
+                    // piece of a segment cut by the warp's sub-slice, kept for the CTA merge:
+                    // slot 0 = the sub-slice's first segment (own buffer), slot 1 = its last
+                    // one, finalised after the last unit, when the warp's ring is idle
+                    const int slot = (t_first == 0) ? 0 : 1;
+                    __syncwarp();
+                    float* pa_acc = slot == 0 ? piece0 + static_cast<uint32_t>(warp) * G * D
+                                              : reinterpret_cast<float*>(ring);
                     if (gid < G) {
 #pragma unroll
                         for (int nn = 0; nn < NT; ++nn)
-                            *reinterpret_cast<float2*>(po + gid * D + nn * 8 + tig * 2) =
-                                make_float2(acc[nn][0] * i0, acc[nn][1] * i0);
-                        if (tig == 0) *reinterpret_cast<float2*>(pml + gid * 2) = make_float2(m0, L0);
+                            *reinterpret_cast<float2*>(pa_acc + gid * D + nn * 8 + tig * 2) =
+                                make_float2(acc[nn][0], acc[nn][1]);
+                        if (tig == 0)
+                            *reinterpret_cast<float2*>(piece_ml + ((warp * 2 + slot) * G + gid) * 2) =
+                                make_float2(m0, L0);
                     }
                     if (gid + 8 < G) {
 #pragma unroll
                         for (int nn = 0; nn < NT; ++nn)
-                            *reinterpret_cast<float2*>(po + (gid + 8) * D + nn * 8 + tig * 2) =
-                                make_float2(acc[nn][2] * i1, acc[nn][3] * i1);
-                        if (tig == 0) *reinterpret_cast<float2*>(pml + (gid + 8) * 2) = make_float2(m1, L1);
+                            *reinterpret_cast<float2*>(pa_acc + (gid + 8) * D + nn * 8 + tig * 2) =
+                                make_float2(acc[nn][2], acc[nn][3]);
+                        if (tig == 0)
+                            *reinterpret_cast<float2*>(piece_ml + ((warp * 2 + slot) * G + gid + 8) * 2) =
+                                make_float2(m1, L1);
                     }
-                    const int32_t w_first = static_cast<int32_t>(slice_owner(seg_a, U, W));
-                    const int32_t w_last = static_cast<int32_t>(slice_owner(seg_b - 1, U, W));
-                    const int32_t expected = (U >= W) ? (w_last - w_first + 1) : (seg_b - seg_a);
-                    __syncwarp();  // the warp's piece stores precede lane 0's release below
-                    int32_t last = 0;
-                    if (lane == 0) last = count_piece(ws.counter + seg_id) == expected - 1;
-                    last = __shfl_sync(0xffffffffu, last, 0);
-                    __syncwarp();  // lane 0's acquire precedes every lane's loads of other pieces
-                    if (last) {
-                        merge_pieces<D>(out + (static_cast<int64_t>(wc.s) * Hq + wc.h * G) * D, seg_a, w_first,
-                                        w_last, U, W, G, ws, lane);
-                        if (lane == 0) ws.counter[seg_id] = 0;
-                    }
+                    if (lane == 0) meta[warp * 2 + slot] = wc.s * num_kv_heads + wc.h;
                 }
             }
             __syncwarp();
@@ -575,6 +579,135 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
         // after an abort: let the copies already issued land before the CTA can exit
         if (consumed < issued && lane == 0) {
             for (int32_t u = consumed; u < issued; ++u) mbar_drain(&bars[u % nst], static_cast<uint32_t>(u / nst) & 1u);
+        }
+    }
+    __syncthreads();
+    if (*abort_flag) return;
+
+    // ---- level 2: merge the pieces of segments cut between this CTA's warps ----------------
+    // A group is the run of pieces of one segment over consecutive warps: a warp's last piece
+    // (slot 1) always starts one (that segment began inside the warp); its first piece (slot 0)
+    // starts one only if no earlier warp of the CTA holds that segment. Each warp merges the
+    // groups that start at its own slots; lane i holds the group's i-th piece.
+    auto warp_len = [&](int32_t w2) {
+        return static_cast<int32_t>((static_cast<int64_t>(w2 + 1) * n_cta) / NW -
+                                    (static_cast<int64_t>(w2) * n_cta) / NW);
+    };
+    for (int32_t s0 = 0; s0 < 2; ++s0) {
+        const int32_t seg = meta[warp * 2 + s0];
+        if (seg < 0) continue;
+        if (s0 == 0) {  // does an earlier warp (skipping empty ones) hold this segment?
+            int32_t w2 = warp - 1;
+            while (w2 >= 0 && warp_len(w2) == 0) --w2;
+            if (w2 >= 0 && (meta[w2 * 2] == seg || meta[w2 * 2 + 1] == seg)) continue;
+        }
+        int32_t my_slot = lane == 0 ? warp * 2 + s0 : -1;
+        int32_t nm = 1;
+        if (!(s0 == 0 && meta[warp * 2 + 1] >= 0)) {  // the segment runs past this warp
+            for (int32_t w2 = warp + 1; w2 < NW; ++w2) {
+                if (warp_len(w2) == 0) continue;
+                if (meta[w2 * 2] != seg) break;
+                if (lane == nm) my_slot = w2 * 2;
+                ++nm;
+                if (meta[w2 * 2 + 1] >= 0) break;  // the segment ends inside warp w2
+            }
+        }
+        const int32_t s = seg / num_kv_heads, h = seg - s * num_kv_heads;
+        const int32_t np = (prefix[s + 1] - prefix[s]) / num_kv_heads;
+        const int32_t seg_a = prefix[s] + h * np, seg_b = seg_a + np;
+        const bool complete = seg_a >= u0 && seg_b <= u1;
+        const int64_t cpiece = static_cast<int64_t>(blockIdx.x) * 2 + (seg_a <= u0 ? 0 : 1);
+        // four heads at a time, their shuffle chains interleaved; pieces hold unnormalised
+        // sums, so piece i weighs 2^(m_i - M) / sum_i l_i 2^(m_i - M)
+        for (int32_t g0 = 0; g0 < G; g0 += 4) {
+            float mk[4], lk[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                mk[k] = -INFINITY;
+                lk[k] = 0.f;
+                if (my_slot >= 0 && g0 + k < G) {
+                    const float2 ml = *reinterpret_cast<const float2*>(piece_ml + (my_slot * G + g0 + k) * 2);
+                    mk[k] = ml.x;
+                    lk[k] = ml.y;
+                }
+            }
+            float Mk[4], dk[4], wk[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) Mk[k] = mk[k];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) Mk[k] = fmaxf(Mk[k], __shfl_xor_sync(0xffffffffu, Mk[k], off));
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                wk[k] = my_slot >= 0 ? exp2f(mk[k] - Mk[k]) : 0.f;
+                dk[k] = lk[k] * wk[k];
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) dk[k] += __shfl_xor_sync(0xffffffffu, dk[k], off);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) wk[k] = __fdividef(wk[k], dk[k]);
+            float v[4][E];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+#pragma unroll
+                for (int e = 0; e < E; ++e) v[k][e] = 0.f;
+            for (int32_t i = 0; i < nm; ++i) {
+                const int32_t si = __shfl_sync(0xffffffffu, my_slot, i);
+                const float* a = ((si & 1) ? reinterpret_cast<const float*>(smem + L.ring + static_cast<uint32_t>(si >> 1) *
+                                                                                              nst * stage_bytes)
+                                           : piece0 + static_cast<uint32_t>(si >> 1) * G * D) +
+                                 lane * E;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float wi = __shfl_sync(0xffffffffu, wk[k], i);
+                    if (g0 + k < G) {
+                        const float* ak = a + (g0 + k) * D;
+                        if constexpr (E == 4) {
+                            const float4 t = *reinterpret_cast<const float4*>(ak);
+                            v[k][0] = fmaf(wi, t.x, v[k][0]); v[k][1] = fmaf(wi, t.y, v[k][1]);
+                            v[k][2] = fmaf(wi, t.z, v[k][2]); v[k][3] = fmaf(wi, t.w, v[k][3]);
+                        } else {
+                            const float2 t = *reinterpret_cast<const float2*>(ak);
+                            v[k][0] = fmaf(wi, t.x, v[k][0]); v[k][1] = fmaf(wi, t.y, v[k][1]);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int32_t g = g0 + k;
+                if (g >= G) continue;
+                if (complete) {
+                    uint32_t* dst =
+                        reinterpret_cast<uint32_t*>(out + (static_cast<int64_t>(s) * Hq + h * G + g) * D + lane * E);
+                    dst[0] = pack_bf16x2(v[k][0], v[k][1]);
+                    if constexpr (E == 4) dst[1] = pack_bf16x2(v[k][2], v[k][3]);
+                } else {
+                    float* dst = ws.piece_o + (cpiece * G + g) * D + lane * E;
+                    if constexpr (E == 4) *reinterpret_cast<float4*>(dst) = make_float4(v[k][0], v[k][1], v[k][2], v[k][3]);
+                    else *reinterpret_cast<float2*>(dst) = make_float2(v[k][0], v[k][1]);
+                    if (lane == 0) *reinterpret_cast<float2*>(ws.piece_ml + (cpiece * G + g) * 2) = make_float2(Mk[k], dk[k]);
+                }
+            }
+        }
+        if (!complete) {
+            // ---- level 3: count this CTA's piece; the last one merges all CTA pieces ----------
+            const int32_t c_first = static_cast<int32_t>(slice_owner(seg_a, U, C));
+            const int32_t c_last = static_cast<int32_t>(slice_owner(seg_b - 1, U, C));
+            const int32_t expected = (U >= C) ? (c_last - c_first + 1) : (seg_b - seg_a);
+            __syncwarp();  // the warp's piece stores precede lane 0's release below
+            int32_t last = 0;
+            if (lane == 0) last = count_piece(ws.counter + seg) == expected - 1;
+            last = __shfl_sync(0xffffffffu, last, 0);
+            __syncwarp();  // lane 0's acquire precedes every lane's loads of other pieces
+            if (last) {
+                merge_pieces<D>(out + (static_cast<int64_t>(s) * Hq + h * G) * D, seg_a, c_first, c_last, U, C, G, ws,
+                                lane);
+                if (lane == 0) ws.counter[seg] = 0;
+            }
         }
     }
 }
@@ -591,8 +724,7 @@ cudaError_t launch_impl(const DecodeArgs& a, const DecodePlan& plan, cudaStream_
     e = cudaFuncSetAttribute(decode_balanced_kernel<D, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(plan.smem_bytes));
     if (e != cudaSuccess) return e;
-    const int32_t W = plan.num_ctas * NW;
-    BalWorkspace ws = bal_ws(a.workspace, a.num_seqs, a.num_kv_heads, G, D, W);
+    BalWorkspace ws = bal_ws(a.workspace, a.num_seqs, a.num_kv_heads, G, D, plan.num_ctas);
 
     // Programmatic launch: the grid may be scheduled while the previous kernel in the stream
     // drains; it waits for that kernel (griddepcontrol.wait) before reading any input.
@@ -629,23 +761,21 @@ int ctas_per_sm(uint32_t smem) {
 bool plan_decode_balanced(int32_t S, int32_t Hkv, int32_t G, int32_t D, const DeviceInfo& dev, DecodePlan* plan) {
     if (G < 4 || G > kBalMaxGroup || (D != 64 && D != 128) || S > kBalMaxSeqs || S < 1) return false;
     const uint32_t stage = bal_stage_bytes(D, G);
-    // Prefer 8 warps per CTA with 2..4 stages each; fall back to 4 warps for large groups.
+    // Prefer 8 streaming warps per CTA with as many stages as fit; 4 warps for large groups.
     for (int NW : {8, 4}) {
         for (int nst = 4; nst >= 2; --nst) {
-            const BalLayout L = bal_layout(NW, nst, stage, S);
+            const BalLayout L = bal_layout(NW, nst, stage, G, D, S);
             if (L.total > static_cast<uint32_t>(dev.max_smem_optin)) continue;
             const int per_sm = (D == 128) ? (NW == 8 ? ctas_per_sm<128, 8>(L.total) : ctas_per_sm<128, 4>(L.total))
                                           : (NW == 8 ? ctas_per_sm<64, 8>(L.total) : ctas_per_sm<64, 4>(L.total));
             if (per_sm < 1) continue;
-            const int ctas = dev.num_sms * per_sm;
-            if (ctas * NW > kBalMaxWarps) continue;
             plan->path = kDecodeMmaBalanced;
             plan->warps = NW;
             plan->stages = nst;
             plan->stage_bytes = stage;
             plan->smem_bytes = L.total;
-            plan->num_ctas = ctas;
-            plan->workspace_bytes = bal_ws_bytes(S, Hkv, G, D, ctas * NW);
+            plan->num_ctas = dev.num_sms * per_sm;
+            plan->workspace_bytes = bal_ws_bytes(S, Hkv, G, D, plan->num_ctas);
             return true;
         }
     }

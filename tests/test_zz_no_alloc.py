@@ -70,8 +70,9 @@ def test_noalloc_matches_pa_decode_on_two_calls(make):
 
 
 def test_noalloc_rejects_shapes_beyond_the_fixed_scratch():
-    # 1024 sequences x 16 q heads per kv head x 8 kv heads needs far more than 16 MiB
-    S, H_q, H_kv, D, msl = 1024, 128, 8, 128, 4096
+    # one merge counter per (sequence, kv head): 1024 x 8192 of them need 32 MiB of scratch
+    S, H_kv, D, msl = 1024, 8192, 64, 256
+    H_q = 4 * H_kv
     assert B.pa_decode_workspace_size(S, H_q, H_kv, D, msl, torch.bfloat16) > B.PA_DECODE_NOALLOC_MAX_BYTES
     lib = B.load()
     dummy = torch.empty(16, dtype=torch.uint8, device="cuda")
