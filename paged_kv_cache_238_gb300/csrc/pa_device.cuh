@@ -85,6 +85,15 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     }
 }
 
+// Bounded wait that ignores the abort flag: used while winding down, to let copies or MMAs
+// already in flight complete before their shared or tensor memory is released.
+__device__ __forceinline__ void mbar_wait_timeout(uint64_t* bar, uint32_t parity) {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > kWaitLimitNs) return;
+    }
+}
+
 // ------------------------------------------------------------------------------------------
 // TMA: 2-D tiled bulk tensor load global -> shared, completion on an mbarrier
 // ------------------------------------------------------------------------------------------

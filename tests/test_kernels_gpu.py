@@ -246,6 +246,23 @@ def test_prefill_small_mixed(dtype, D):
     assert_close(out, ref, dtype, f"prefill {dtype} D{D}")
 
 
+@pytest.mark.parametrize("G,H_kv", [(1, 2), (2, 2), (4, 2), (8, 1), (16, 1)])
+def test_prefill_tensor_core_groups_and_ragged_tiles(G, H_kv):
+    """bf16 / head_dim 128 runs the tcgen05 kernel: 128-row query tiles of 128/G tokens x G
+    heads, 128-key tiles. Chunks that end mid-tile, prior context that ends mid-block and
+    crosses several key tiles, and a chunk that starts at position 0."""
+    wl = W.build_mixed(82 + G, prior_lens=[0, 1, 127, 300, 1000], chunk_lens=[200, 37, 129, 64, 300],
+                       decode_lens=[9], H_q=G * H_kv, H_kv=H_kv, D=128, num_blocks=400, dtype="bf16",
+                       pad_multiple=64)
+    dw = DeviceWorkload(wl)
+    run_reshape(dw)
+    out = run_prefill(dw)
+    kc, vc = dw.host_pool_after_writes()
+    ref = oracle.attention(wl.q_prefill, kc, vc, wl.block_table_prefill, wl.seq_lens_prefill, wl.scale,
+                           query_start_loc=wl.query_start_loc)
+    assert_close(out, ref, "bf16", f"tensor-core prefill G{G}")
+
+
 def test_prefill_empty_chunks_and_whole_prompt():
     wl = W.build_mixed(81, prior_lens=[10, 0, 3], chunk_lens=[0, 40, 0], decode_lens=[5], H_q=4, H_kv=1, D=128,
                        num_blocks=32, dtype="bf16", pad_multiple=0)
