@@ -18,6 +18,10 @@ e2e    = the same metric with every step's inputs copied host->device from pinne
          its output copied back, inside the timed graph.
 --impl reference  times the fp64 CPU oracle (test infrastructure) on a bounded sample of the
          same workload and prints the same line with "impl": "reference".
+--workload  measures another workload of the same path instead of the GQA decode batch:
+         prefix_sharing (aliased prefix blocks), long_split_kv (8 x 32768 tokens) or
+         mixed_step (reshape_and_cache of 8448 slots + chunked prefill + 240-sequence decode;
+         its line reports new tokens/s and, per kernel, the HBM or tensor-pipe roofline).
 """
 from __future__ import annotations
 
@@ -41,59 +45,131 @@ METRIC = "paged-KV decode attention: achieved HBM TB/s vs peak; seqs/s (bs 64, G
 WORKLOAD = "GQA decode bf16: 64 seqs, 32 q / 8 kv heads, head_dim 128, block 16, lognormal lengths (mean ~195, " \
            "clipped 16-2048), shuffled physical blocks, 4096-block pool, reshape_and_cache of 1 new token per seq"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 L2_BYTES = 129 * 1024 * 1024
 
 
 # ------------------------------------------------------------------------------------------
-# workload bytes (algorithmic, per step)
+# workloads and their algorithmic work (per step)
 # ------------------------------------------------------------------------------------------
 
-def step_bytes(wl) -> dict:
+#: name -> (builder name in workloads, description, default steps, KV replicas rotated)
+WORKLOADS = {
+    "gqa_decode": ("gqa_decode", WORKLOAD, 20000, 10),
+    "prefix_sharing": ("prefix_sharing",
+                       "Prefix-sharing decode bf16: 128 seqs, first 1024 tokens alias the same 64 physical blocks, "
+                       "unique suffix U{0..512}, 32 q / 8 kv heads, head_dim 128, block 16, 8192-block pool", 5000, 3),
+    "long_split_kv": ("long_split_kv",
+                      "Long-context split-KV decode bf16: 8 seqs x 32768 tokens, 64 q / 8 kv heads, head_dim 128, "
+                      "block 16, 20000-block pool, one new token per seq", 2000, 1),
+    "mixed_step": ("mixed_step",
+                   "Mixed step bf16: 16 chunked-prefill seqs of 512 new tokens on prior context U{0..4096} + 240 "
+                   "decode seqs with context U{64..4096}, 32 q / 8 kv heads, head_dim 128, block 16, slot_mapping "
+                   "for all new tokens padded to 8448 with padding slots in the null block", 300, 1),
+}
+
+
+def _kv_token_bytes(wl) -> int:
     el = 2 if wl.dtype == "bf16" else 4
-    lens = wl.seq_lens.astype(np.int64)
-    kv = int(lens.sum()) * 2 * wl.H_kv * wl.D * el
-    q = wl.S * wl.H_q * wl.D * el
-    out = q
-    bt = int(np.sum(-(-lens // 16))) * 4
-    seq = wl.S * 4
-    T = 0 if wl.slot_mapping is None else wl.slot_mapping.shape[0]
-    new = 2 * T * wl.H_kv * wl.D * el          # new K and V read ...
-    k1 = 2 * new + 8 * T                       # ... and written, plus the slots
-    decode = kv + q + out + bt + seq
-    return {"kv": kv, "decode": decode, "reshape": k1, "step": decode + k1}
+    return 2 * wl.H_kv * wl.D * el
+
+
+def step_bytes(wl) -> dict:
+    """Algorithmic bytes of one step: every visible key's K and V once, Q and output, the
+    block-table entries a kernel must read, lengths, and the new tokens' K/V read and written
+    (plus their slots). Prefill flops count visible (query, key) pairs only."""
+    el = 2 if wl.dtype == "bf16" else 4
+    tok = _kv_token_bytes(wl)
+    res = {"decode": 0, "prefill": 0, "reshape": 0, "kv": 0, "prefill_flops": 0, "kv_unique": 0}
+    if wl.seq_lens is not None and wl.S > 0:
+        lens = wl.seq_lens.astype(np.int64)
+        kv = int(lens.sum()) * tok
+        q = wl.S * wl.H_q * wl.D * el
+        bt = int(np.sum(-(-lens // 16))) * 4
+        res["decode"] = kv + 2 * q + bt + wl.S * 4
+        res["kv"] += kv
+        # distinct (block, row) pairs actually holding visible keys: aliased prefixes count once
+        seen = {}
+        for i in range(wl.S):
+            n = int(lens[i])
+            for j in range(-(-n // 16)):
+                b = int(wl.block_table[i, j])
+                seen[b] = max(seen.get(b, 0), min(16, n - 16 * j))
+        res["kv_unique"] += sum(seen.values()) * tok
+    if wl.seq_lens_prefill is not None:
+        L = wl.seq_lens_prefill.astype(np.int64)
+        C = np.diff(wl.query_start_loc).astype(np.int64)
+        kv = int(L.sum()) * tok
+        Tp = int(C.sum())
+        q = Tp * wl.H_q * wl.D * el
+        bt = int(np.sum(-(-L // 16))) * 4
+        res["prefill"] = kv + 2 * q + bt + 4 * (2 * len(L) + 1)
+        res["kv"] += kv
+        res["kv_unique"] += kv
+        pairs = int(np.sum((L - C) * C + C * (C + 1) // 2))
+        res["prefill_flops"] = 4 * wl.D * wl.H_q * pairs
+    if wl.slot_mapping is not None:
+        T = wl.slot_mapping.shape[0]
+        new = T * tok                               # new K and V read ...
+        res["reshape"] = 2 * new + 8 * T            # ... and written, plus the slots
+    res["step"] = res["decode"] + res["prefill"] + res["reshape"]
+    return res
+
+
+def _peaks_file() -> dict:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            return json.load(fh)
+    except Exception:
+        return {}
 
 
 def load_peaks() -> tuple:
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    try:
-        with open(path) as fh:
-            p = json.load(fh)
+    """HBM copy bandwidth (GB/s) measured on this GPU model, else the fallback figure."""
+    p = _peaks_file()
+    if "hbm_gbs" in p:
         return float(p["hbm_gbs"]), "measured"
-    except Exception:
-        return FALLBACK_HBM_GBS, "fallback"
+    return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+def load_tensor_peak() -> tuple:
+    """Dense bf16 tensor throughput (TFLOP/s): the measured burst figure (a kernel timed
+    between memory-bound kernels, not a seconds-long GEMM loop), else the fallback."""
+    p = _peaks_file()
+    if "bf16_tflops" in p:
+        return float(p["bf16_tflops"]), "measured (burst)"
+    return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+#: sources each kernel is built from (a recorded ncu traffic figure is valid only for them)
+KERNEL_SOURCES = {
+    "decode": ("decode.cu", "decode_balanced.cu", "pa_device.cuh"),
+    "prefill": ("prefill.cu", "pa_tcgen05.cuh", "pa_device.cuh"),
+    "reshape": ("reshape_and_cache.cu", "pa_device.cuh"),
+}
+
+
+def kernel_source_hash(kernel: str = "decode") -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_238_gb300", "csrc")
-    for f in ("decode.cu", "decode_balanced.cu", "pa_device.cuh"):
+    for f in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic() -> "float | None":
-    """DRAM bytes per decode launch from the committed ncu summary, if it was taken on the
-    current decode kernel source (null otherwise)."""
-    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+def recorded_traffic(kernel: str = "decode", workload: str = "gqa_decode") -> "float | None":
+    """DRAM bytes (read + written) per launch of `kernel` on `workload`, from the committed ncu
+    summary, if it was taken on the kernel's current source (null otherwise)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as fh:
-            rec = json.load(fh)
+            rec = json.load(fh).get(f"{kernel}/{workload}")
     except Exception:
         return None
-    if rec.get("kernel_source_hash") != kernel_source_hash():
+    if not rec or rec.get("kernel_source_hash") != kernel_source_hash(kernel):
         return None
-    return rec.get("dram_bytes_per_decode_call")
+    return rec.get("dram_bytes_per_launch")
 
 
 # ------------------------------------------------------------------------------------------
@@ -180,30 +256,160 @@ def count_launches_per_step(step_fn) -> "int | None":
             step_fn(0)
             torch.cuda.synchronize()
         names = [e.name for e in prof.events() if e.device_type == torch.autograd.DeviceType.CUDA]
-        ours = [n for n in names if "pa::" in n or "reshape_and_cache" in n or "decode_" in n]
+        ours = [n for n in names if "pa::" in n or "reshape_and_cache" in n or "decode_" in n or "prefill_" in n]
         return len(ours) if ours else None
     except Exception:
         return None
 
 
-def cpu_baseline(wl, budget_s: float = 10.0) -> dict:
-    """The fp64 oracle (test infrastructure), as it stands, on the host cores: full 64-seq
-    passes of the same step until ~budget_s of CPU time."""
+def _subset(wl, n_dec: int, n_pre: int):
+    """The first n_dec decode and n_pre prefill sequences of a workload, with their new tokens."""
+    from paged_kv_cache_238_gb300 import workloads as W
+    d = dict(wl.__dict__)
+    if wl.seq_lens is not None:
+        d.update(q=wl.q[:n_dec], block_table=wl.block_table[:n_dec], seq_lens=wl.seq_lens[:n_dec])
+    tok = []
+    if wl.seq_lens_prefill is not None:
+        qsl = wl.query_start_loc[:n_pre + 1]
+        d.update(q_prefill=wl.q_prefill[:qsl[-1]], block_table_prefill=wl.block_table_prefill[:n_pre],
+                 seq_lens_prefill=wl.seq_lens_prefill[:n_pre], query_start_loc=qsl)
+        tok.append(np.arange(int(qsl[-1])))
+    if wl.slot_mapping is not None:
+        # decode workloads: one new token per sequence, in sequence order; mixed: the prefill
+        # chunks' tokens first, then one per decode sequence, then padding
+        if wl.seq_lens_prefill is not None:
+            tok.append(int(wl.query_start_loc[-1]) + np.arange(n_dec))
+        else:
+            tok.append(np.arange(n_dec))
+        idx = np.concatenate(tok)
+        d.update(k_new=wl.k_new[idx], v_new=wl.v_new[idx], slot_mapping=wl.slot_mapping[idx])
+    return W.Workload(**d)
+
+
+def _oracle_pass(wl, cores: int):
     import oracle
-    kc, vc = wl.k_cache.copy(), wl.v_cache.copy()
+    kc, vc = wl.k_cache, wl.v_cache
+    if wl.slot_mapping is not None and wl.slot_mapping.shape[0] > 0:
+        oracle.reshape_and_cache(wl.k_new, wl.v_new, kc, vc, wl.slot_mapping)
+    if wl.seq_lens_prefill is not None and len(wl.seq_lens_prefill) > 0:
+        oracle.attention(wl.q_prefill, kc, vc, wl.block_table_prefill, wl.seq_lens_prefill, wl.scale,
+                         query_start_loc=wl.query_start_loc, num_threads=cores)
+    if wl.seq_lens is not None and wl.S > 0:
+        oracle.attention(wl.q, kc, vc, wl.block_table, wl.seq_lens, wl.scale, num_threads=cores)
+
+
+def oracle_sample(wl, budget_s: float):
+    """A bounded sample of one step of the workload for the fp64 oracle: the largest leading
+    fraction of its sequences (decode and prefill alike) whose oracle pass fits ~budget_s."""
     cores = os.cpu_count() or 1
-    b = step_bytes(wl)["step"]
+    n_dec = wl.S if wl.seq_lens is not None else 0
+    n_pre = len(wl.seq_lens_prefill) if wl.seq_lens_prefill is not None else 0
+    p_dec, p_pre = min(n_dec, 1), min(n_pre, 1)
+    t0 = time.perf_counter()
+    _oracle_pass(_subset(wl, p_dec, p_pre), cores)
+    one = time.perf_counter() - t0
+    # a probe of one decode and one prefill sequence; scale by the larger count
+    est_full = one * max(n_dec, n_pre, 1)
+    frac = 1.0 if est_full <= budget_s else budget_s / est_full
+    sd = n_dec if frac >= 1 else max(p_dec, int(n_dec * frac))
+    sp = n_pre if frac >= 1 else max(p_pre, int(n_pre * frac))
+    return _subset(wl, sd, sp), sd, sp, cores
+
+
+def cpu_baseline(wl, budget_s: float = 10.0, value_key: str = "step") -> dict:
+    """The fp64 oracle (test infrastructure), as it stands, on the host cores, over a bounded
+    sample of one step of the same workload, repeated until ~budget_s."""
+    sub, sd, sp, cores = oracle_sample(wl, budget_s / 2)
+    b = step_bytes(sub)
     passes, t0 = 0, time.perf_counter()
     while True:
-        oracle.reshape_and_cache(wl.k_new, wl.v_new, kc, vc, wl.slot_mapping)
-        oracle.attention(wl.q, kc, vc, wl.block_table, wl.seq_lens, wl.scale, num_threads=cores)
+        _oracle_pass(sub, cores)
         passes += 1
         if time.perf_counter() - t0 > budget_s or passes >= 50:
             break
     dt = time.perf_counter() - t0
-    return {"value": b * passes / dt / 1e12, "unit": "TB/s", "cores": cores, "kind": "oracle",
-            "sample": f"{passes} full passes of the 64-sequence step (reshape_and_cache + decode) in {dt:.1f} s",
-            "seqs_per_s": wl.S * passes / dt}
+    tokens = sd + (int(sub.query_start_loc[-1]) if sp else 0)
+    res = {"unit": "TB/s", "cores": cores, "kind": "oracle",
+           "sample": f"{passes} passes over {sd} decode + {sp} prefill sequences of one step "
+                     f"(reshape_and_cache + attention, fp64) in {dt:.1f} s",
+           "seqs_per_s": (sd + sp) * passes / dt, "tokens_per_s": tokens * passes / dt}
+    if value_key == "tokens":
+        res["value"], res["unit"] = tokens * passes / dt, "tokens/s"
+    else:
+        res["value"] = b["step"] * passes / dt / 1e12
+    return res
+
+
+class DeviceStep:
+    """The workload's device tensors (R rotated KV pools) and one step of the hot path:
+    reshape_and_cache of the step's new tokens, then chunked prefill and decode attention."""
+
+    def __init__(self, wl, dev, R: int, stream):
+        import torch
+        from paged_kv_cache_238_gb300 import binding as B
+        self.B, self.wl, self.stream, self.R = B, wl, stream, R
+        kc0, vc0 = to_dev(wl.k_cache, dev), to_dev(wl.v_cache, dev)
+        self.kcs = [kc0] + [kc0.clone() for _ in range(R - 1)]
+        self.vcs = [vc0] + [vc0.clone() for _ in range(R - 1)]
+        self.has_new = wl.slot_mapping is not None and wl.slot_mapping.shape[0] > 0
+        self.has_dec = wl.seq_lens is not None and wl.S > 0
+        self.has_pre = wl.seq_lens_prefill is not None and len(wl.seq_lens_prefill) > 0
+        self.inputs, self.outputs = [], []
+        if self.has_new:
+            self.k_new, self.v_new, self.slots = (to_dev(wl.k_new, dev), to_dev(wl.v_new, dev),
+                                                  to_dev(wl.slot_mapping, dev))
+            self.inputs += [self.k_new, self.v_new, self.slots]
+        if self.has_dec:
+            self.q, self.bt, self.lens = to_dev(wl.q, dev), to_dev(wl.block_table, dev), to_dev(wl.seq_lens, dev)
+            self.out = torch.empty_like(self.q)
+            self.msl = int(wl.seq_lens.max())
+            dt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+            self.ws = torch.zeros(max(16, B.pa_decode_workspace_size(wl.S, wl.H_q, wl.H_kv, wl.D, self.msl, dt)),
+                                  dtype=torch.uint8, device=dev)
+            self.inputs += [self.q, self.bt, self.lens]
+            self.outputs.append(self.out)
+        if self.has_pre:
+            self.qp = to_dev(wl.q_prefill, dev)
+            self.btp, self.lp = to_dev(wl.block_table_prefill, dev), to_dev(wl.seq_lens_prefill, dev)
+            self.qsl = to_dev(wl.query_start_loc, dev)
+            self.outp = torch.empty_like(self.qp)
+            self.max_chunk = int(np.diff(wl.query_start_loc).max())
+            self.msl_p = int(wl.seq_lens_prefill.max())
+            self.inputs += [self.qp, self.btp, self.lp, self.qsl]
+            self.outputs.append(self.outp)
+        self.kernels = [k for k, on in (("reshape", self.has_new), ("prefill", self.has_pre),
+                                        ("decode", self.has_dec)) if on]
+
+    def __call__(self, i: int, ev=None):
+        """Step i on pool i % R; ev maps a kernel name to an event pair recorded around it."""
+        B, r, s, wl = self.B, i % self.R, self.stream, self.wl
+
+        def rec(k, j):
+            if ev is not None and k in ev:
+                ev[k][j].record(s)
+
+        if self.has_new:
+            rec("reshape", 0)
+            B.pa_reshape_and_cache(self.k_new, self.v_new, self.kcs[r], self.vcs[r], self.slots, stream=s)
+            rec("reshape", 1)
+        if self.has_pre:
+            rec("prefill", 0)
+            B.pa_prefill_chunk(self.outp, self.qp, self.kcs[r], self.vcs[r], self.btp, self.lp, self.qsl,
+                               self.max_chunk, self.msl_p, wl.scale, stream=s)
+            rec("prefill", 1)
+        if self.has_dec:
+            rec("decode", 0)
+            B.pa_decode(self.out, self.q, self.kcs[r], self.vcs[r], self.bt, self.lens, self.msl, wl.scale,
+                        self.ws, stream=s)
+            rec("decode", 1)
+
+
+KERNEL_LABEL = {
+    "decode": "pa_decode: balanced TMA + mma.sync decode kernel (split merge in-kernel)",
+    "prefill": "pa_prefill_chunk: tcgen05 chunked-prefill kernel (TMA page gather, S/O/P in TMEM)",
+    "reshape": "pa_reshape_and_cache: slot scatter",
+}
+MIXED_METRIC = "mixed step: new tokens/s (16 x 512-token prefill chunks + 240 decode seqs)"
 
 
 def run_ours(args):
@@ -219,31 +425,14 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
-    wl = W.gqa_decode()
+    builder, desc, _, _ = WORKLOADS[args.workload]
+    wl = getattr(W, builder)()
     nbytes = step_bytes(wl)
     R = args.replicas
-    # one pool per layer: contents come from the generator; replicas are device copies
-    kc0, vc0 = to_dev(wl.k_cache, dev), to_dev(wl.v_cache, dev)
-    kcs = [kc0] + [kc0.clone() for _ in range(R - 1)]
-    vcs = [vc0] + [vc0.clone() for _ in range(R - 1)]
-    q, k_new, v_new = to_dev(wl.q, dev), to_dev(wl.k_new, dev), to_dev(wl.v_new, dev)
-    slots, bt, lens = to_dev(wl.slot_mapping, dev), to_dev(wl.block_table, dev), to_dev(wl.seq_lens, dev)
-    out = torch.empty_like(q)
-    msl = int(wl.seq_lens.max())
-    ws = torch.zeros(max(16, B.pa_decode_workspace_size(wl.S, wl.H_q, wl.H_kv, wl.D, msl, torch.bfloat16)),
-                     dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
+    step = DeviceStep(wl, dev, R, stream)
 
-    def step(i, ev=None):
-        r = i % R
-        B.pa_reshape_and_cache(k_new, v_new, kcs[r], vcs[r], slots, stream=stream)
-        if ev is not None:
-            ev[0].record(stream)
-        B.pa_decode(out, q, kcs[r], vcs[r], bt, lens, msl, wl.scale, ws, stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
-
-    # ---- warm-up (eager, untimed) and a parity spot-check of one sequence --------------------
+    # ---- warm-up (eager, untimed) ----------------------------------------------------------
     with torch.cuda.stream(stream):
         for i in range(max(args.warmup, 3)):
             step(i)
@@ -251,59 +440,49 @@ def run_ours(args):
     assert B.pa_get_device_errors(clear=True) == 0
     launches_per_step = None if args.no_cupti else count_launches_per_step(step)
     if launches_per_step is None:
-        launches_per_step = 2  # reshape_and_cache + the balanced decode kernel (split merge inside)
+        launches_per_step = len(step.kernels)  # one kernel per call (split merge inside decode)
 
     # ---- capture K steps in graphs -------------------------------------------------------
     K = args.steps
     chunk = min(K, args.graph_chunk)
-    ev_pairs = [(torch.cuda.Event(enable_timing=True, external=True),
-                 torch.cuda.Event(enable_timing=True, external=True)) for _ in range(chunk)]
 
-    def capture(n, with_events):
+    def evpair():
+        return (torch.cuda.Event(enable_timing=True, external=True),
+                torch.cuda.Event(enable_timing=True, external=True))
+
+    ev_steps = [{k: evpair() for k in step.kernels} for _ in range(chunk)]
+
+    def capture(fn, n, with_events):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
             with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
                 for i in range(n):
-                    step(i, ev_pairs[i] if with_events else None)
+                    if with_events:
+                        fn(i, ev_steps[i])
+                    else:
+                        fn(i)
         return g
 
-    g_main = capture(chunk, True)
+    g_main = capture(step, chunk, True)
     rem = K % chunk
-    g_rem = capture(rem, False) if rem else None
+    g_rem = capture(step, rem, False) if rem else None
     n_main = K // chunk
 
-    # ---- e2e graph: pinned host inputs in, result out, every step -------------------------
-    h_q = q.cpu().pin_memory()
-    h_kn, h_vn = k_new.cpu().pin_memory(), v_new.cpu().pin_memory()
-    h_slots, h_bt, h_lens = slots.cpu().pin_memory(), bt.cpu().pin_memory(), lens.cpu().pin_memory()
-    h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_kn, h_vn, h_slots, h_bt, h_lens))
-    d2h = h_out.numel() * h_out.element_size()
+    # ---- e2e graph: pinned host inputs in, results out, every step ------------------------
+    h_in = [t.cpu().pin_memory() for t in step.inputs]
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in step.outputs]
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
 
     def e2e_step(i):
-        r = i % R
-        for d, h in ((q, h_q), (k_new, h_kn), (v_new, h_vn), (slots, h_slots), (bt, h_bt), (lens, h_lens)):
+        for d, h in zip(step.inputs, h_in):
             d.copy_(h, non_blocking=True)
-        B.pa_reshape_and_cache(k_new, v_new, kcs[r], vcs[r], slots, stream=stream)
-        B.pa_decode(out, q, kcs[r], vcs[r], bt, lens, msl, wl.scale, ws, stream=stream)
-        h_out.copy_(out, non_blocking=True)
+        step(i)
+        for h, d in zip(h_out, step.outputs):
+            h.copy_(d, non_blocking=True)
 
-    def capture_e2e(n):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
-                for i in range(n):
-                    e2e_step(i)
-        return g
-
-    g_e2e = capture_e2e(chunk)
-    g_e2e_rem = capture_e2e(rem) if rem else None
-
-    def run_graphs(gm, gr):
-        for _ in range(n_main):
-            gm.replay()
-        if gr is not None:
-            gr.replay()
+    g_e2e = capture(e2e_step, chunk, False)
+    g_e2e_rem = capture(e2e_step, rem, False) if rem else None
 
     def timed(gm, gr):
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -312,7 +491,10 @@ def run_ours(args):
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
             t0.record(stream)
-            run_graphs(gm, gr)
+            for _ in range(n_main):
+                gm.replay()
+            if gr is not None:
+                gr.replay()
             t1.record(stream)
         torch.cuda.synchronize()
         if world > 1:
@@ -334,42 +516,74 @@ def run_ours(args):
             stream.synchronize()
     ms_total = timed(g_main, g_rem)
     clocks = sampler.stop()
-    # per-call decode duration from the last replay of the main graph (inside the timed region)
-    dec_ms = [a.elapsed_time(b) for a, b in ev_pairs]
-    dec_avg_ms = sum(dec_ms) / len(dec_ms)
+    # per-kernel durations from the last replay of the main graph (inside the timed region)
+    kern_ms = {k: sum(e[k][0].elapsed_time(e[k][1]) for e in ev_steps) / chunk for k in step.kernels}
     ms_e2e = timed(g_e2e, g_e2e_rem)
     assert B.pa_get_device_errors(clear=True) == 0
 
     ms_step = ms_total / K
-    value = nbytes["step"] * world / (ms_step * 1e-3) / 1e12
-    e2e_value = nbytes["step"] * world / (ms_e2e / K * 1e-3) / 1e12
-    peak, peak_kind = load_peaks()
-    achieved_gbs = nbytes["decode"] / (dec_avg_ms * 1e-3) / 1e9
+    hbm_peak, hbm_kind = load_peaks()
+    tc_peak, tc_kind = load_tensor_peak()
+    kernels = {}
+    for k, ms in kern_ms.items():
+        if k == "prefill":
+            ach = nbytes["prefill_flops"] / (ms * 1e-3) / 1e12
+            kernels[k] = {"us": round(ms * 1e3, 3), "bound": "tensor", "achieved": round(ach, 1), "unit": "TFLOP/s",
+                          "peak": tc_peak, "frac": round(ach / tc_peak, 4), "peak_source": tc_kind,
+                          "hbm_gbs": round(nbytes["prefill"] / (ms * 1e-3) / 1e9, 1)}
+        else:
+            ach = nbytes[k] / (ms * 1e-3) / 1e9
+            kernels[k] = {"us": round(ms * 1e3, 3), "bound": "hbm", "achieved": round(ach, 1), "unit": "GB/s",
+                          "peak": hbm_peak, "frac": round(ach / hbm_peak, 4), "peak_source": hbm_kind}
+    dom = max(kern_ms, key=kern_ms.get)
+    roof = {"kernel": KERNEL_LABEL[dom], **{k: v for k, v in kernels[dom].items() if k != "us"},
+            "kernel_us": kernels[dom]["us"], "traffic": recorded_traffic(dom, args.workload)}
+    if dom == "decode":
+        roof["decode_call_us"] = kernels[dom]["us"]
+
+    n_seqs = (wl.S if step.has_dec else 0) + (len(wl.seq_lens_prefill) if step.has_pre else 0)
+    tokens = (wl.S if step.has_dec else 0) + (int(wl.query_start_loc[-1]) if step.has_pre else 0)
+    if args.workload == "mixed_step":
+        metric, unit, nd = MIXED_METRIC, "tokens/s", 1
+        value = tokens * world / (ms_step * 1e-3)
+        e2e_value = tokens * world / (ms_e2e / K * 1e-3)
+    else:
+        metric, unit, nd = METRIC, "TB/s", 4
+        value = nbytes["step"] * world / (ms_step * 1e-3) / 1e12
+        e2e_value = nbytes["step"] * world / (ms_e2e / K * 1e-3) / 1e12
     line = {
-        "metric": METRIC, "value": round(value, 4), "unit": "TB/s", "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": round(ms_step, 6), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded generator; no dataset)",
-        "config": {"workload": WORKLOAD, "seqs": wl.S, "mean_len": round(float(wl.seq_lens.mean()), 2),
-                   "keys": int(wl.seq_lens.sum()), "bytes_per_step": nbytes["step"],
-                   "decode_bytes_per_call": nbytes["decode"], "kv_layers_rotated": R,
-                   "l2": f"inputs larger than L2: {R} KV pools rotated, each touched again only after "
-                         f"{(R - 1) * nbytes['step'] / 1e6:.0f} MB of other pools (L2 {L2_BYTES / 1e6:.0f} MB)",
+        "metric": metric, "value": round(value, nd), "unit": unit, "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded generator; no dataset)",
+        "config": {"workload": desc, "seqs": n_seqs, "keys": int(nbytes["kv"] // _kv_token_bytes(wl)),
+                   "bytes_per_step": nbytes["step"], "kernels_per_step": step.kernels, "kv_pools_rotated": R,
+                   "l2": f"inputs larger than L2: {R} KV pool(s) rotated, "
+                         f"{R * nbytes['kv_unique'] / 1e6:.0f} MB of distinct KV touched per rotation "
+                         f"(L2 {L2_BYTES / 1e6:.0f} MB)",
                    "graph": f"{n_main} x {chunk}-step CUDA graph" + (f" + {rem}-step graph" if rem else ""),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
-        "seqs_per_s": round(wl.S * world / (ms_step * 1e-3), 1),
-        "tokens_per_s": round(wl.S * world / (ms_step * 1e-3), 1),
-        "e2e": {"value": round(e2e_value, 4), "unit": "TB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(ms_e2e / K, 6)},
-        "roofline": {"kernel": "pa_decode: balanced TMA + mma.sync decode kernel (split merge in-kernel)",
-                     "bound": "hbm",
-                     "achieved": round(achieved_gbs, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved_gbs / peak, 4), "peak_source": peak_kind,
-                     "decode_call_us": round(dec_avg_ms * 1e3, 3), "traffic": recorded_traffic()},
+        "seqs_per_s": round(n_seqs * world / (ms_step * 1e-3), 1),
+        "tokens_per_s": round(tokens * world / (ms_step * 1e-3), 1),
+        "e2e": {"value": round(e2e_value, nd), "unit": unit, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e / K, 6)},
+        "roofline": roof,
+        "kernels": kernels,
         "gpu_launches": launches_per_step * K,
         "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
     }
+    if args.workload == "gqa_decode":
+        line["config"]["decode_bytes_per_call"] = nbytes["decode"]
+        line["config"]["mean_len"] = round(float(wl.seq_lens.mean()), 2)
+    if nbytes["kv_unique"] < nbytes["kv"]:
+        # aliased prefix blocks: the logical bytes count each sequence's keys; DRAM sees the
+        # distinct blocks once (the rest is served from L2)
+        line["config"]["kv_bytes_logical"] = nbytes["kv"]
+        line["config"]["kv_bytes_distinct"] = nbytes["kv_unique"]
+        line["decode_distinct_hbm_frac"] = round(
+            (nbytes["decode"] - nbytes["kv"] + nbytes["kv_unique"]) / (kern_ms["decode"] * 1e-3) / 1e9 / hbm_peak, 4)
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_budget_s)
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_budget_s, "tokens" if unit == "tokens/s" else "step")
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -384,46 +598,38 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    import oracle
     from paged_kv_cache_238_gb300 import workloads as W
 
-    wl = W.gqa_decode()
-    cores = os.cpu_count() or 1
-    kc, vc = wl.k_cache.copy(), wl.v_cache.copy()
+    builder, desc, _, _ = WORKLOADS[args.workload]
+    wl = getattr(W, builder)()
     # Size each step's sample so the whole run stays within ~budget seconds.
-    t0 = time.perf_counter()
-    oracle.reshape_and_cache(wl.k_new, wl.v_new, kc, vc, wl.slot_mapping)
-    oracle.attention(wl.q, kc, vc, wl.block_table, wl.seq_lens, wl.scale, num_threads=cores)
-    full_s = time.perf_counter() - t0
     per_step_budget = args.reference_budget_s / max(1, args.steps + args.warmup)
-    n_seq = int(max(1, min(wl.S, wl.S * per_step_budget / max(full_s, 1e-9))))
-    idx = np.arange(n_seq)
-    sub = W.Workload(**{**wl.__dict__, "q": wl.q[idx], "block_table": wl.block_table[idx],
-                        "seq_lens": wl.seq_lens[idx], "k_new": wl.k_new[idx], "v_new": wl.v_new[idx],
-                        "slot_mapping": wl.slot_mapping[idx]})
-    b = step_bytes(sub)["step"]
-
-    def one():
-        oracle.reshape_and_cache(sub.k_new, sub.v_new, kc, vc, sub.slot_mapping)
-        oracle.attention(sub.q, kc, vc, sub.block_table, sub.seq_lens, sub.scale, num_threads=cores)
-
+    sub, sd, sp, cores = oracle_sample(wl, per_step_budget)
+    b = step_bytes(sub)
+    tokens = sd + (int(sub.query_start_loc[-1]) if sp else 0)
     for _ in range(args.warmup):
-        one()
+        _oracle_pass(sub, cores)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        one()
+        _oracle_pass(sub, cores)
     dt = time.perf_counter() - t0
-    value = b * args.steps / dt / 1e12
-    threads = min(cores, n_seq)
+    if args.workload == "mixed_step":
+        metric, unit = MIXED_METRIC, "tokens/s"
+        value = tokens * args.steps / dt
+    else:
+        metric, unit = METRIC, "TB/s"
+        value = b["step"] * args.steps / dt / 1e12
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TB/s", "n_gpus": world,
+        "impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded generator; no dataset)",
-        "config": {"workload": WORKLOAD, "sample_seqs_per_step": n_seq},
-        "seqs_per_s": n_seq * args.steps / dt,
-        "cpu_baseline": {"value": value, "unit": "TB/s", "cores": threads, "kind": "oracle",
-                         "sample": f"{n_seq} of the 64 sequences per step (reshape_and_cache + decode), fp64"},
-        "e2e": {"value": value, "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "config": {"workload": desc, "sample_decode_seqs_per_step": sd, "sample_prefill_seqs_per_step": sp},
+        "seqs_per_s": (sd + sp) * args.steps / dt,
+        "tokens_per_s": tokens * args.steps / dt,
+        "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
+                         "sample": f"{sd} decode + {sp} prefill sequences of the step per timed step "
+                                   f"(reshape_and_cache + attention), fp64"},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
@@ -431,10 +637,12 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="gqa_decode",
+                    help="the GQA decode batch (default) or another workload of the same path")
+    ap.add_argument("--steps", type=int, default=None, help="timed steps (default: per workload)")
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--replicas", type=int, default=10, help="KV pools rotated across steps")
+    ap.add_argument("--replicas", type=int, default=None, help="KV pools rotated across steps (default: per workload)")
     ap.add_argument("--graph-chunk", type=int, default=500, help="steps per captured graph")
     ap.add_argument("--preheat-s", type=float, default=1.0)
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
@@ -442,6 +650,11 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-cupti", action="store_true", help="skip the activity-trace launch count (e.g. under ncu)")
     args = ap.parse_args(argv)
+    _, _, default_steps, default_replicas = WORKLOADS[args.workload]
+    if args.steps is None:
+        args.steps = default_steps
+    if args.replicas is None:
+        args.replicas = default_replicas
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
