@@ -8,9 +8,9 @@ lengths with mean ~195, 16-token blocks, shuffled physical blocks).
 Timing: the step's device inputs stay resident; steps rotate through R independent KV pools
 (one per "layer", the same block table), so a pool is touched again only after the other
 R-1 (> 3 x L2 in between): inputs larger than L2, no flush kernel. K steps are captured in
-CUDA graphs (the step is launch-bound at ~10 us) and timed with CUDA events on the launching
-stream, barrier + synchronize on both sides, max over ranks. Each decode call is bracketed
-by its own event pair inside the graph; the roofline figure uses their average.
+CUDA graphs (a step is ~20 us, so launches matter) and timed with CUDA events on the launching
+stream, barrier + synchronize on both sides, max over ranks. Every 50th step of a graph
+brackets each of its kernels with an event pair; the roofline figure uses their average.
 
 value  = algorithmic bytes of the step / step time (TB/s): KV bytes of every visible key,
          Q, output, block-table entries, lengths, and the new tokens' K/V read and written.
@@ -450,14 +450,18 @@ def run_ours(args):
         return (torch.cuda.Event(enable_timing=True, external=True),
                 torch.cuda.Event(enable_timing=True, external=True))
 
-    ev_steps = [{k: evpair() for k in step.kernels} for _ in range(chunk)]
+    # Event pairs around each kernel on every `sample`-th step of the graph only: an event node
+    # splits the programmatic (early-launch) edge between two kernels, so bracketing every
+    # kernel of every step would slow the steps the line reports.
+    sample = max(1, min(args.event_every, chunk))
+    ev_steps = {i: {k: evpair() for k in step.kernels} for i in range(0, chunk, sample)}
 
     def capture(fn, n, with_events):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
             with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
                 for i in range(n):
-                    if with_events:
+                    if with_events and i in ev_steps:
                         fn(i, ev_steps[i])
                     else:
                         fn(i)
@@ -516,8 +520,10 @@ def run_ours(args):
             stream.synchronize()
     ms_total = timed(g_main, g_rem)
     clocks = sampler.stop()
-    # per-kernel durations from the last replay of the main graph (inside the timed region)
-    kern_ms = {k: sum(e[k][0].elapsed_time(e[k][1]) for e in ev_steps) / chunk for k in step.kernels}
+    # per-kernel durations from the sampled steps of the last replay of the main graph (inside
+    # the timed region)
+    kern_ms = {k: sum(e[k][0].elapsed_time(e[k][1]) for e in ev_steps.values()) / len(ev_steps)
+               for k in step.kernels}
     ms_e2e = timed(g_e2e, g_e2e_rem)
     assert B.pa_get_device_errors(clear=True) == 0
 
@@ -562,6 +568,8 @@ def run_ours(args):
                          f"{R * nbytes['kv_unique'] / 1e6:.0f} MB of distinct KV touched per rotation "
                          f"(L2 {L2_BYTES / 1e6:.0f} MB)",
                    "graph": f"{n_main} x {chunk}-step CUDA graph" + (f" + {rem}-step graph" if rem else ""),
+                   "kernel_timing": f"CUDA event pairs around each kernel of every {sample}th step of the timed "
+                                    f"graph ({len(ev_steps)} per replay)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "seqs_per_s": round(n_seqs * world / (ms_step * 1e-3), 1),
         "tokens_per_s": round(tokens * world / (ms_step * 1e-3), 1),
@@ -644,6 +652,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--replicas", type=int, default=None, help="KV pools rotated across steps (default: per workload)")
     ap.add_argument("--graph-chunk", type=int, default=500, help="steps per captured graph")
+    ap.add_argument("--event-every", type=int, default=50, help="time each kernel on every Nth step of a graph")
     ap.add_argument("--preheat-s", type=float, default=1.0)
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
     ap.add_argument("--reference-budget-s", type=float, default=90.0)

@@ -11,8 +11,9 @@
 //
 // Streaming. Each warp is an independent worker with its own ring of stages in shared memory.
 // Lane 0 resolves a page's physical block through the block table ("My Understanding of vLLM
-// and PagedAttention", "Block Table") and issues the page's K and V as 2-D TMA tile copies
-// (128-byte swizzle, 64-column boxes) completing on the stage's mbarrier; when the unit starts
+// and PagedAttention", "Block Table") and issues the page's K and V as one TMA tile copy each
+// (128-byte swizzle; at head_dim 128 a 3-D box of 64 columns x 16 rows x 2 column halves, so the
+// page lands as two 2 KB swizzled halves) completing on the stage's mbarrier; when the unit starts
 // a new segment it also bulk-copies that segment's G query rows into the stage. Block ids are
 // fetched 32 units ahead by the warp's lanes. The warp consumes a stage (S = Q K^T and
 // O += P V on mma.sync m16n8k16 with the G q heads that share a kv head as rows, so each page
@@ -369,10 +370,12 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
                 uint8_t* stage = ring + static_cast<uint32_t>(st) * stage_bytes;
                 const uint32_t qbytes = static_cast<uint32_t>(G) * D * 2u;
                 mbar_arrive_expect_tx(&bars[st], 2u * kPage + (seg_first ? qbytes : 0u));
-#pragma unroll
-                for (uint32_t hf = 0; hf < kHalves; ++hf) {
-                    tma_load_2d_hint(stage + hf * 2048u, &tm_k, hf * 64, row, &bars[st], kv_policy);
-                    tma_load_2d_hint(stage + kPage + hf * 2048u, &tm_v, hf * 64, row, &bars[st], kv_policy);
+                if constexpr (kHalves == 2) {  // both 64-column halves in one box
+                    tma_load_3d_hint(stage, &tm_k, 0, row, 0, &bars[st], kv_policy);
+                    tma_load_3d_hint(stage + kPage, &tm_v, 0, row, 0, &bars[st], kv_policy);
+                } else {
+                    tma_load_2d_hint(stage, &tm_k, 0, row, &bars[st], kv_policy);
+                    tma_load_2d_hint(stage + kPage, &tm_v, 0, row, &bars[st], kv_policy);
                 }
                 if (seg_first) {
                     bulk_copy_g2s(stage + 2u * kPage, q + (static_cast<int64_t>(wi.s) * Hq + wi.h * G) * D, qbytes,
@@ -716,9 +719,18 @@ template <int D, int NW>
 cudaError_t launch_impl(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream) {
     alignas(64) CUtensorMap tm_k, tm_v;
     const uint64_t rows = static_cast<uint64_t>(a.num_blocks) * a.num_kv_heads * kBlock;
-    cudaError_t e = encode_bf16_2d_sw128(&tm_k, a.k_cache, D, rows, 64, kBlock);
-    if (e != cudaSuccess) return e;
-    e = encode_bf16_2d_sw128(&tm_v, a.v_cache, D, rows, 64, kBlock);
+    cudaError_t e;
+    if (D == 128) {
+        // (column within a half, pool row, half): one box is a whole 16-row page, stored as
+        // two 16 x 128-byte swizzled halves
+        e = encode_bf16_3d_sw128(&tm_k, a.k_cache, 64, rows, 2, D * 2, 128, 64, kBlock, 2);
+        if (e != cudaSuccess) return e;
+        e = encode_bf16_3d_sw128(&tm_v, a.v_cache, 64, rows, 2, D * 2, 128, 64, kBlock, 2);
+    } else {
+        e = encode_bf16_2d_sw128(&tm_k, a.k_cache, D, rows, 64, kBlock);
+        if (e != cudaSuccess) return e;
+        e = encode_bf16_2d_sw128(&tm_v, a.v_cache, D, rows, 64, kBlock);
+    }
     if (e != cudaSuccess) return e;
     const int32_t G = a.num_q_heads / a.num_kv_heads;
     e = cudaFuncSetAttribute(decode_balanced_kernel<D, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize,

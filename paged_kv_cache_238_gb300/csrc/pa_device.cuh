@@ -86,12 +86,14 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 }
 
 // Bounded wait that ignores the abort flag: used while winding down, to let copies or MMAs
-// already in flight complete before their shared or tensor memory is released.
-__device__ __forceinline__ void mbar_wait_timeout(uint64_t* bar, uint32_t parity) {
+// already in flight complete before their shared or tensor memory is released. Returns
+// whether the phase completed in time.
+__device__ __forceinline__ bool mbar_wait_timeout(uint64_t* bar, uint32_t parity) {
     const uint64_t t0 = global_timer_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (global_timer_ns() - t0 > kWaitLimitNs) return;
+        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
     }
+    return true;
 }
 
 // ------------------------------------------------------------------------------------------
@@ -113,6 +115,15 @@ __device__ __forceinline__ void tma_load_2d_hint(void* smem_dst, const void* ten
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, "
         "{%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
         "l"(tensor_map), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_hint(void* smem_dst, const void* tensor_map, int32_t c0, int32_t c1,
+                                                 int32_t c2, uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, "
+        "{%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(smem_dst)),
+        "l"(tensor_map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
 

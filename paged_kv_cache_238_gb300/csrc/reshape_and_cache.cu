@@ -24,6 +24,10 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const int4* __re
                                                                 uint32_t num_items, uint32_t chunks_per_row,
                                                                 uint32_t num_kv_heads, int64_t num_slots,
                                                                 uint32_t* err) {
+    // Programmatic launch: wait for the kernel before this one (it may still read the pool or
+    // produce k, v and the slots), then let the next kernel's grid be scheduled.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const uint32_t stride = gridDim.x * blockDim.x;
     for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < num_items; i += stride) {
         const uint32_t row = i / chunks_per_row;          // (token, head)
@@ -58,12 +62,21 @@ cudaError_t launch_reshape_and_cache(const ReshapeArgs& a, int num_sms, cudaStre
     int64_t blocks = (num_items + threads - 1) / threads;
     const int64_t cap = static_cast<int64_t>(num_sms) * 8;
     if (blocks > cap) blocks = cap;
-    reshape_and_cache_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
-        static_cast<const int4*>(a.k), static_cast<const int4*>(a.v), static_cast<int4*>(a.k_cache),
-        static_cast<int4*>(a.v_cache), a.slot_mapping, static_cast<uint32_t>(num_items),
-        static_cast<uint32_t>(chunks_per_row), static_cast<uint32_t>(a.num_kv_heads),
-        static_cast<int64_t>(a.num_blocks) * kBlock, a.err);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, reshape_and_cache_kernel, static_cast<const int4*>(a.k),
+                              static_cast<const int4*>(a.v), static_cast<int4*>(a.k_cache),
+                              static_cast<int4*>(a.v_cache), a.slot_mapping, static_cast<uint32_t>(num_items),
+                              static_cast<uint32_t>(chunks_per_row), static_cast<uint32_t>(a.num_kv_heads),
+                              static_cast<int64_t>(a.num_blocks) * kBlock, a.err);
 }
 
 }  // namespace pa

@@ -121,7 +121,7 @@ def test_mixed_step_decode_rows_sampled():
 # ----------------------------------------------------------------------------- decode: edge cases
 
 @pytest.mark.parametrize("lens", [[1, 15, 16, 17, 31, 32, 33], [16] * 9, [2048, 1, 700], [5] * 300])
-@pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("G", [1, 2, 4, 5, 6, 8, 16])
 def test_decode_ragged_lengths_and_groups(lens, G):
     H_kv = 2 if G <= 8 else 1
     need = sum(-(-L // 16) for L in lens) + 2
