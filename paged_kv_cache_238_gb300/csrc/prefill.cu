@@ -9,7 +9,9 @@
 // heads that share the kv head, so every K/V tile is read once for the whole group. Keys go in
 // tiles of 128 (eight 16-token blocks gathered through the block table):
 //   warp 0   - producer: resolves block ids 32 pages ahead and issues 2-D TMA tile copies
-//              (128-byte swizzle) of the tile's K and V pages into 3-stage rings;
+//              (128-byte swizzle) of the tile's K and V pages into 3-stage rings, sixteen
+//              lanes at once (page x column half), since one thread issuing every copy in
+//              turn cannot keep up with the tensor cores;
 //   warp 1   - owns the tensor memory (512 columns: two S buffers and O in fp32, two P buffers
 //              in bf16) and issues, from one thread, S = Q K^T (both operands in shared memory)
 //              and O += P V (P from tensor memory) as tcgen05.mma kind::f16 (M = N = 128,
@@ -47,7 +49,7 @@ struct TcSmem {
     static constexpr uint32_t k = q + kTile;                 // kTcStages stages
     static constexpr uint32_t v = k + kTcStages * kTile;     // kTcStages stages
     static constexpr uint32_t bars = v + kTcStages * kTile;
-    static constexpr int kNumBars = 4 * kTcStages + 7;
+    static constexpr int kNumBars = 4 * kTcStages + 8;
     static constexpr uint32_t misc = bars + kNumBars * 8;  // tmem base, abort flag
     static constexpr uint32_t total = misc + 16 + 1024;
 };
@@ -86,12 +88,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
     uint64_t* p_full = s_full + 2;                 // [2] P written to TMEM, S read (4 softmax warps)
     uint64_t* pv_done = p_full + 2;                // [2] PV of the tile finished (commit)
     uint64_t* idle = pv_done + 2;                  // every MMA issued has finished (final commit)
+    uint64_t* q_full = idle + 1;                   // Q tile stored in shared memory (128 softmax threads)
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + TcSmem::misc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + TcSmem::misc + 4);
 
     const int32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int32_t seq = blockIdx.x, h = blockIdx.y;
-    const int32_t tile = gridDim.z - 1 - blockIdx.z;  // the longest tiles start first
+    // Query tiles of one (sequence, kv head) are adjacent in launch order, so they run at the
+    // same time and read each K/V tile from L2 after the first of them brings it in.
+    const int32_t seq = blockIdx.z, h = blockIdx.y;
+    const int32_t tile = gridDim.x - 1 - blockIdx.x;  // the longest tiles start first
     const int32_t Hq = G * num_kv_heads;
     const int32_t q0 = __ldg(query_start_loc + seq);
     const int32_t C = __ldg(query_start_loc + seq + 1) - q0;
@@ -113,26 +118,40 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
         for (int i = 0; i < TcSmem::kNumBars; ++i) mbar_init(&bars[i], 1);
         mbar_init(&p_full[0], 4);
         mbar_init(&p_full[1], 4);
+        mbar_init(q_full, kTcThreads - 64);
         fence_mbarrier_init();
     }
     if (warp == 1) {
         umma::tmem_alloc(tmem_holder, 512);
         umma::tmem_relinquish();
     }
-    // ---- Q tile: row r = token * G + head, bounds-checked 16-byte loads into the swizzled
-    // K-major layout (two 64-column halves); rows past the chunk are zero
-    for (int32_t i = tid; i < kTcRows * 16; i += kTcThreads) {
-        const int32_t r = i >> 4, c16 = i & 15;  // row, 16-byte chunk of the 256-byte row
-        const int32_t t = t0 + r / G, g = r % G;
-        int4 v = make_int4(0, 0, 0, 0);
-        if (t < C) v = *reinterpret_cast<const int4*>(q + (static_cast<int64_t>(q0 + t) * Hq + h * G + g) * kTcD + c16 * 8);
-        *reinterpret_cast<int4*>(smem + TcSmem::q + (c16 >> 3) * kHalf + sw128_offset(r, c16 & 7)) = v;
-    }
-    fence_proxy_async_shared();
     umma::fence_before_sync();
-    __syncthreads();
+    __syncthreads();  // barriers initialised, tensor memory allocated: the producer starts now
     umma::fence_after_sync();
     const uint32_t tmem = *tmem_holder;
+    if (warp >= 2) {
+        // ---- Q tile, by the softmax threads while the first K/V copies are in flight: row
+        // r = token * G + head, 16-byte loads (all issued before any store) into the swizzled
+        // K-major layout (two 64-column halves); rows past the chunk are zero
+        constexpr int kPer = kTcRows * 16 / (kTcThreads - 64);
+        int4 v[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int32_t i = (tid - 64) + k * (kTcThreads - 64);
+            const int32_t r = i >> 4, c16 = i & 15;  // row, 16-byte chunk of the 256-byte row
+            const int32_t t = t0 + r / G, g = r % G;
+            v[k] = make_int4(0, 0, 0, 0);
+            if (t < C) v[k] = *reinterpret_cast<const int4*>(q + (static_cast<int64_t>(q0 + t) * Hq + h * G + g) * kTcD + c16 * 8);
+        }
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int32_t i = (tid - 64) + k * (kTcThreads - 64);
+            const int32_t r = i >> 4, c16 = i & 15;
+            *reinterpret_cast<int4*>(smem + TcSmem::q + (c16 >> 3) * kHalf + sw128_offset(r, c16 & 7)) = v[k];
+        }
+        fence_proxy_async_shared();  // generic stores before the tensor core reads them
+        mbar_arrive(q_full);
+    }
     // tensor memory columns: S buffers at 0 and 128 (fp32), O at 256 (fp32), P buffers at 384
     // and 448 (bf16 pairs)
     const uint32_t tmem_o = tmem + 256, tmem_p = tmem + 384;
@@ -175,12 +194,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
             uint8_t* sk = smem + TcSmem::k + st * kTile;
             if (lane == 0) mbar_arrive_expect_tx(&k_full[st], kTile);
             last_k = j;
-            for (int k = 0; k < 8; ++k) {
-                const int32_t rk = __shfl_sync(0xffffffffu, row_cur, (j & 3) * 8 + k);
-                if (lane == 0) {
-                    tma_load_2d(sk + k * 2048u, &tm_k, 0, rk, &k_full[st]);
-                    tma_load_2d(sk + kHalf + k * 2048u, &tm_k, 64, rk, &k_full[st]);
-                }
+            {
+                const int32_t rk = __shfl_sync(0xffffffffu, row_cur, (j & 3) * 8 + (lane & 7));
+                __syncwarp();
+                if (lane < 16)
+                    tma_load_2d(sk + (lane >> 3) * kHalf + (lane & 7) * 2048u, &tm_k, (lane >> 3) * 64, rk, &k_full[st]);
             }
             // V of tile j: its stage is free once PV of tile j - stages is done
             if (use > 0 && lane == 0) ok = wait_or_abort(&v_empty[st], (use - 1) & 1u, abort_flag, err);
@@ -189,12 +207,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
             uint8_t* sv = smem + TcSmem::v + st * kTile;
             if (lane == 0) mbar_arrive_expect_tx(&v_full[st], kTile);
             last_v = j;
-            for (int k = 0; k < 8; ++k) {
-                const int32_t rk = __shfl_sync(0xffffffffu, row_cur, (j & 3) * 8 + k);
-                if (lane == 0) {
-                    tma_load_2d(sv + k * 2048u, &tm_v, 0, rk, &v_full[st]);
-                    tma_load_2d(sv + kHalf + k * 2048u, &tm_v, 64, rk, &v_full[st]);
-                }
+            {
+                const int32_t rk = __shfl_sync(0xffffffffu, row_cur, (j & 3) * 8 + (lane & 7));
+                __syncwarp();
+                if (lane < 16)
+                    tma_load_2d(sv + (lane >> 3) * kHalf + (lane & 7) * 2048u, &tm_v, (lane >> 3) * 64, rk, &v_full[st]);
             }
         }
     } else if (warp == 1) {
@@ -218,7 +235,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
                 umma::commit(&k_empty[st]);
                 return true;
             };
-            bool ok = issue_qk(0);
+            bool ok = wait_or_abort(q_full, 0, abort_flag, err);
+            if (ok) ok = issue_qk(0);
             if (ok && n_kv > 1) ok = issue_qk(1);
             for (int32_t j = 0; j < n_kv && ok; ++j) {
                 const int32_t b = j & 1, st = j % kTcStages;
@@ -417,7 +435,7 @@ cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     constexpr int TT = kTcRows / G;
     const int32_t tiles = (a.max_chunk_len + TT - 1) / TT;
-    dim3 grid(a.num_seqs, a.num_kv_heads, tiles);
+    dim3 grid(tiles, a.num_kv_heads, a.num_seqs);
     prefill_tc_kernel<G><<<grid, kTcThreads, TcSmem::total, stream>>>(
         tm_k, tm_v, static_cast<__nv_bfloat16*>(a.out), static_cast<const __nv_bfloat16*>(a.q), a.block_table,
         a.max_blocks_per_seq, a.seq_lens, a.query_start_loc, a.num_kv_heads, a.num_blocks, a.scale * kLog2e, a.err);
@@ -429,7 +447,7 @@ cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t stream) {
 cudaError_t launch_prefill(const PrefillArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
     const int32_t G = a.num_q_heads / a.num_kv_heads;
     const bool tc = a.dtype == PA_BF16 && a.head_dim == kTcD && (G == 1 || G == 2 || G == 4 || G == 8 || G == 16) &&
-                    a.num_kv_heads <= 65535 && (a.max_chunk_len + kTcRows / G - 1) / (kTcRows / G) <= 65535 &&
+                    a.num_kv_heads <= 65535 && a.num_seqs <= 65535 &&
                     static_cast<int>(TcSmem::total) <= dev.max_smem_optin;
     if (tc) {
         switch (G) {
