@@ -21,7 +21,8 @@ e2e    = the same metric with every step's inputs copied host->device from pinne
 --workload  measures another workload of the same path instead of the GQA decode batch:
          prefix_sharing (aliased prefix blocks), long_split_kv (8 x 32768 tokens) or
          mixed_step (reshape_and_cache of 8448 slots + chunked prefill + 240-sequence decode;
-         its line reports new tokens/s and, per kernel, the HBM or tensor-pipe roofline).
+         its line reports new tokens/s and, per kernel, the HBM or tensor-pipe roofline) or
+         prefill_chunks (the mixed step's prefill half alone, in TFLOP/s).
 """
 from __future__ import annotations
 
@@ -53,7 +54,7 @@ L2_BYTES = 129 * 1024 * 1024
 # workloads and their algorithmic work (per step)
 # ------------------------------------------------------------------------------------------
 
-#: name -> (builder name in workloads, description, default steps, KV replicas rotated)
+#: name -> (builder in workloads: name or (name, kwargs), description, default steps, KV replicas rotated)
 WORKLOADS = {
     "gqa_decode": ("gqa_decode", WORKLOAD, 20000, 10),
     "prefix_sharing": ("prefix_sharing",
@@ -66,7 +67,17 @@ WORKLOADS = {
                    "Mixed step bf16: 16 chunked-prefill seqs of 512 new tokens on prior context U{0..4096} + 240 "
                    "decode seqs with context U{64..4096}, 32 q / 8 kv heads, head_dim 128, block 16, slot_mapping "
                    "for all new tokens padded to 8448 with padding slots in the null block", 300, 1),
+    "prefill_chunks": (("mixed_step", {"n_decode": 0, "num_blocks": 0}),
+                       "Chunked prefill bf16: the mixed step's 16 chunks of 512 new tokens on prior context "
+                       "U{0..4096}, 32 q / 8 kv heads, head_dim 128, block 16, pool sized to those sequences", 300, 1),
 }
+
+
+def build_workload(name: str):
+    from paged_kv_cache_238_gb300 import workloads as W
+    builder = WORKLOADS[name][0]
+    fn, kw = (builder, {}) if isinstance(builder, str) else builder
+    return getattr(W, fn)(**kw)
 
 
 def _kv_token_bytes(wl) -> int:
@@ -335,6 +346,8 @@ def cpu_baseline(wl, budget_s: float = 10.0, value_key: str = "step") -> dict:
            "seqs_per_s": (sd + sp) * passes / dt, "tokens_per_s": tokens * passes / dt}
     if value_key == "tokens":
         res["value"], res["unit"] = tokens * passes / dt, "tokens/s"
+    elif value_key == "flops":
+        res["value"], res["unit"] = b["prefill_flops"] * passes / dt / 1e12, "TFLOP/s"
     else:
         res["value"] = b["step"] * passes / dt / 1e12
     return res
@@ -410,6 +423,7 @@ KERNEL_LABEL = {
     "reshape": "pa_reshape_and_cache: slot scatter",
 }
 MIXED_METRIC = "mixed step: new tokens/s (16 x 512-token prefill chunks + 240 decode seqs)"
+PREFILL_METRIC = "chunked prefill: causal attention TFLOP/s (16 x 512-token chunks, GQA 32/8, head_dim 128)"
 
 
 def run_ours(args):
@@ -425,8 +439,8 @@ def run_ours(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
-    builder, desc, _, _ = WORKLOADS[args.workload]
-    wl = getattr(W, builder)()
+    desc = WORKLOADS[args.workload][1]
+    wl = build_workload(args.workload)
     nbytes = step_bytes(wl)
     R = args.replicas
     stream = torch.cuda.Stream(device=dev)
@@ -553,6 +567,10 @@ def run_ours(args):
         metric, unit, nd = MIXED_METRIC, "tokens/s", 1
         value = tokens * world / (ms_step * 1e-3)
         e2e_value = tokens * world / (ms_e2e / K * 1e-3)
+    elif args.workload == "prefill_chunks":
+        metric, unit, nd = PREFILL_METRIC, "TFLOP/s", 2
+        value = nbytes["prefill_flops"] * world / (ms_step * 1e-3) / 1e12
+        e2e_value = nbytes["prefill_flops"] * world / (ms_e2e / K * 1e-3) / 1e12
     else:
         metric, unit, nd = METRIC, "TB/s", 4
         value = nbytes["step"] * world / (ms_step * 1e-3) / 1e12
@@ -591,7 +609,8 @@ def run_ours(args):
         line["decode_distinct_hbm_frac"] = round(
             (nbytes["decode"] - nbytes["kv"] + nbytes["kv_unique"]) / (kern_ms["decode"] * 1e-3) / 1e9 / hbm_peak, 4)
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_budget_s, "tokens" if unit == "tokens/s" else "step")
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_budget_s,
+                                            {"tokens/s": "tokens", "TFLOP/s": "flops"}.get(unit, "step"))
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -608,8 +627,8 @@ def run_reference(args):
         return
     from paged_kv_cache_238_gb300 import workloads as W
 
-    builder, desc, _, _ = WORKLOADS[args.workload]
-    wl = getattr(W, builder)()
+    desc = WORKLOADS[args.workload][1]
+    wl = build_workload(args.workload)
     # Size each step's sample so the whole run stays within ~budget seconds.
     per_step_budget = args.reference_budget_s / max(1, args.steps + args.warmup)
     sub, sd, sp, cores = oracle_sample(wl, per_step_budget)
@@ -624,6 +643,9 @@ def run_reference(args):
     if args.workload == "mixed_step":
         metric, unit = MIXED_METRIC, "tokens/s"
         value = tokens * args.steps / dt
+    elif args.workload == "prefill_chunks":
+        metric, unit = PREFILL_METRIC, "TFLOP/s"
+        value = step_bytes(sub)["prefill_flops"] * args.steps / dt / 1e12
     else:
         metric, unit = METRIC, "TB/s"
         value = b["step"] * args.steps / dt / 1e12

@@ -37,6 +37,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, ui
            ((M >> 4) << 24);
 }
 
+// One lane of the (fully active) warp, chosen by the hardware; the others get false.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.b32 %0, 1, 0, P;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // ------------------------------------------------------------------------------------------
 // TMEM allocation (one warp, whole-warp instructions)
 // ------------------------------------------------------------------------------------------

@@ -38,7 +38,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kTcD = 128;
 constexpr int kTcRows = 128;       // query rows per tile (M)
 constexpr int kTcKeys = 128;       // keys per tile (N of S = Q K^T, K of O += P V)
-constexpr int kTcThreads = 192;    // producer warp, MMA warp, 4 softmax warps
+constexpr int kTcThreads = 224;    // K producer, MMA warp, 4 softmax warps, V producer
+constexpr int kSoftmaxThreads = 128;  // warps 2-5
+constexpr int kVWarp = 6;
 constexpr uint32_t kHalf = 16384;  // 128 rows x 128 bytes (64 bf16 columns)
 constexpr uint32_t kTile = 2 * kHalf;  // a 128 x 128 bf16 operand
 constexpr float kRescaleThreshold = 8.f;  // log2 units
@@ -118,7 +120,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
         for (int i = 0; i < TcSmem::kNumBars; ++i) mbar_init(&bars[i], 1);
         mbar_init(&p_full[0], 4);
         mbar_init(&p_full[1], 4);
-        mbar_init(q_full, kTcThreads - 64);
+        mbar_init(q_full, kSoftmaxThreads);
         fence_mbarrier_init();
     }
     if (warp == 1) {
@@ -129,15 +131,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
     __syncthreads();  // barriers initialised, tensor memory allocated: the producer starts now
     umma::fence_after_sync();
     const uint32_t tmem = *tmem_holder;
-    if (warp >= 2) {
+    if (warp >= 2 && warp < kVWarp) {
         // ---- Q tile, by the softmax threads while the first K/V copies are in flight: row
         // r = token * G + head, 16-byte loads (all issued before any store) into the swizzled
         // K-major layout (two 64-column halves); rows past the chunk are zero
-        constexpr int kPer = kTcRows * 16 / (kTcThreads - 64);
+        constexpr int kPer = kTcRows * 16 / kSoftmaxThreads;
         int4 v[kPer];
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
-            const int32_t i = (tid - 64) + k * (kTcThreads - 64);
+            const int32_t i = (tid - 64) + k * kSoftmaxThreads;
             const int32_t r = i >> 4, c16 = i & 15;  // row, 16-byte chunk of the 256-byte row
             const int32_t t = t0 + r / G, g = r % G;
             v[k] = make_int4(0, 0, 0, 0);
@@ -145,7 +147,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
         }
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
-            const int32_t i = (tid - 64) + k * (kTcThreads - 64);
+            const int32_t i = (tid - 64) + k * kSoftmaxThreads;
             const int32_t r = i >> 4, c16 = i & 15;
             *reinterpret_cast<int4*>(smem + TcSmem::q + (c16 >> 3) * kHalf + sw128_offset(r, c16 & 7)) = v[k];
         }
@@ -156,13 +158,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
     // and 448 (bf16 pairs)
     const uint32_t tmem_o = tmem + 256, tmem_p = tmem + 384;
 
-    int32_t last_k = -1, last_v = -1;  // producer: last key tile whose K / V copies were issued
-    if (warp == 0) {
-        // ================================ producer ========================================
-        if (lane == 0) {
-            prefetch_tensormap(&tm_k);
-            prefetch_tensormap(&tm_v);
-        }
+    int32_t last_j = -1;  // producers: last key tile whose copies this warp issued
+    if (warp == 0 || warp == kVWarp) {
+        // ============================ producers: K (warp 0), V ===============================
+        // Separate warps, so that K copies never wait for a V stage to be freed (V stages
+        // are released later, after P V) and run as far ahead as their own ring allows.
+        const bool is_v = warp == kVWarp;
+        const void* tm = is_v ? static_cast<const void*>(&tm_v) : static_cast<const void*>(&tm_k);
+        uint64_t* full = is_v ? v_full : k_full;
+        uint64_t* empty = is_v ? v_empty : k_empty;
+        uint8_t* ring = smem + (is_v ? TcSmem::v : TcSmem::k);
+        if (lane == 0) prefetch_tensormap(tm);
         // block ids, 32 pages (four key tiles) per window: lane i holds page 32 w + i; the
         // next window is fetched while the current one is issued
         auto page_row = [&](int32_t pg) -> int32_t {
@@ -186,53 +192,50 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
                 row_cur = row_nxt;
                 row_nxt = page_row(32 * (win + 1) + lane);
             }
-            // K of tile j: its stage is free once QK of tile j - stages is done
+            // tile j's stage is free once the MMA of tile j - stages that read it is done
             bool ok = true;
-            if (use > 0 && lane == 0) ok = wait_or_abort(&k_empty[st], (use - 1) & 1u, abort_flag, err);
+            if (use > 0 && lane == 0) ok = wait_or_abort(&empty[st], (use - 1) & 1u, abort_flag, err);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
-            uint8_t* sk = smem + TcSmem::k + st * kTile;
-            if (lane == 0) mbar_arrive_expect_tx(&k_full[st], kTile);
-            last_k = j;
-            {
-                const int32_t rk = __shfl_sync(0xffffffffu, row_cur, (j & 3) * 8 + (lane & 7));
-                __syncwarp();
-                if (lane < 16)
-                    tma_load_2d(sk + (lane >> 3) * kHalf + (lane & 7) * 2048u, &tm_k, (lane >> 3) * 64, rk, &k_full[st]);
-            }
-            // V of tile j: its stage is free once PV of tile j - stages is done
-            if (use > 0 && lane == 0) ok = wait_or_abort(&v_empty[st], (use - 1) & 1u, abort_flag, err);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            uint8_t* sv = smem + TcSmem::v + st * kTile;
-            if (lane == 0) mbar_arrive_expect_tx(&v_full[st], kTile);
-            last_v = j;
-            {
-                const int32_t rk = __shfl_sync(0xffffffffu, row_cur, (j & 3) * 8 + (lane & 7));
-                __syncwarp();
-                if (lane < 16)
-                    tma_load_2d(sv + (lane >> 3) * kHalf + (lane & 7) * 2048u, &tm_v, (lane >> 3) * 64, rk, &v_full[st]);
-            }
+            uint8_t* dst = ring + st * kTile;
+            if (lane == 0) mbar_arrive_expect_tx(&full[st], kTile);
+            last_j = j;
+            const int32_t rk = __shfl_sync(0xffffffffu, row_cur, (j & 3) * 8 + (lane & 7));
+            __syncwarp();
+            if (lane < 16)  // lane = (column half, page): 16 copies issued at once
+                tma_load_2d(dst + (lane >> 3) * kHalf + (lane & 7) * 2048u, tm, (lane >> 3) * 64, rk, &full[st]);
         }
     } else if (warp == 1) {
         // ================================ MMA issuer =======================================
-        if (lane == 0) {
+        // The whole warp follows the schedule, so every operand stays warp-uniform; one lane,
+        // elected once, issues every tcgen05 instruction (a commit tracks only the MMAs of the
+        // thread that issues it).
+        {
+            const bool leader = umma::elect_one();
             const uint32_t idesc_qk = umma::idesc_bf16_f32(128, 128, 0, 0);  // Q, K both K-major
             const uint32_t idesc_pv = umma::idesc_bf16_f32(128, 128, 0, 1);  // P (TMEM), V MN-major
-            const uint32_t sq = smem_u32(smem + TcSmem::q);
+            // Descriptors are built once and stepped by adding the byte offset / 16 to their
+            // start-address field (no carry: every shared address here is below 2^18); building
+            // them per instruction costs the single issuing thread more than the MMA itself.
+            const uint64_t dq = umma::smem_desc_sw128(smem_u32(smem + TcSmem::q), 16, 1024);
+            const uint64_t dk0 = umma::smem_desc_sw128(smem_u32(smem + TcSmem::k), 16, 1024);
+            const uint64_t dv0 = umma::smem_desc_sw128(smem_u32(smem + TcSmem::v), kHalf, 1024);
             auto issue_qk = [&](int32_t j) -> bool {
                 const int32_t b = j & 1, st = j % kTcStages;
                 if (!wait_or_abort(&k_full[st], static_cast<uint32_t>(j / kTcStages) & 1u, abort_flag, err)) return false;
                 umma::fence_after_sync();
-                const uint32_t sk = smem_u32(smem + TcSmem::k + st * kTile);
+                const uint64_t dk = dk0 + static_cast<uint64_t>(st) * (kTile >> 4);
+                const uint32_t d_s = tmem + b * 128;
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
-                    const uint32_t off = (ks >> 2) * kHalf + (ks & 3) * 32;
-                    umma::mma_bf16(tmem + b * 128, umma::smem_desc_sw128(sq + off, 16, 1024),
-                                   umma::smem_desc_sw128(sk + off, 16, 1024), idesc_qk, ks > 0);
+                    const uint64_t off = ((ks >> 2) * kHalf + (ks & 3) * 32) >> 4;
+                    if (leader) umma::mma_bf16(d_s, dq + off, dk + off, idesc_qk, ks > 0);
                 }
-                umma::commit(&s_full[b]);
-                umma::commit(&k_empty[st]);
+                if (leader) {
+                    umma::commit(&s_full[b]);
+                    umma::commit(&k_empty[st]);
+                }
+                __syncwarp();
                 return true;
             };
             bool ok = wait_or_abort(q_full, 0, abort_flag, err);
@@ -244,21 +247,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
                 if (ok) ok = wait_or_abort(&v_full[st], static_cast<uint32_t>(j / kTcStages) & 1u, abort_flag, err);
                 if (!ok) break;
                 umma::fence_after_sync();
-                const uint32_t sv = smem_u32(smem + TcSmem::v + st * kTile);
+                const uint64_t dv = dv0 + static_cast<uint64_t>(st) * (kTile >> 4);
+                const uint32_t a_p = tmem_p + b * 64;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {  // 16 keys per instruction: 8 P columns
-                    umma::mma_bf16_tmem_a(tmem_o, tmem_p + b * 64 + kk * 8,
-                                          umma::smem_desc_sw128(sv + kk * 2048u, kHalf, 1024), idesc_pv,
-                                          (j > 0 || kk > 0));
+                    if (leader)
+                        umma::mma_bf16_tmem_a(tmem_o, a_p + kk * 8, dv + static_cast<uint64_t>(kk * (2048 >> 4)),
+                                              idesc_pv, (j > 0 || kk > 0));
                 }
-                umma::commit(&pv_done[b]);
-                umma::commit(&v_empty[st]);
+                if (leader) {
+                    umma::commit(&pv_done[b]);
+                    umma::commit(&v_empty[st]);
+                }
+                __syncwarp();
                 if (j + 2 < n_kv) ok = issue_qk(j + 2);
             }
-            umma::commit(idle);  // arrives once every MMA issued above has finished
+            if (leader) umma::commit(idle);  // arrives once every MMA issued above has finished
+            __syncwarp();
         }
-        __syncwarp();
-    } else {
+    } else if (warp < kVWarp) {
         // ================================ softmax warps ===================================
         const int32_t quad = warp & 3;                 // TMEM lane quadrant of this warp
         const int32_t r = quad * 32 + lane;            // query row of this thread
@@ -407,13 +414,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
     }
 
     // ---- wind down: copies landed and MMAs retired before shared and tensor memory go ------
-    if (warp == 0 && lane == 0) {
-        for (int32_t j = max(0, last_k - kTcStages + 1); j <= last_k; ++j)
-            mbar_wait_timeout(&k_full[j % kTcStages], static_cast<uint32_t>(j / kTcStages) & 1u);
-        for (int32_t j = max(0, last_v - kTcStages + 1); j <= last_v; ++j)
-            mbar_wait_timeout(&v_full[j % kTcStages], static_cast<uint32_t>(j / kTcStages) & 1u);
+    if ((warp == 0 || warp == kVWarp) && lane == 0) {
+        uint64_t* full = warp == kVWarp ? v_full : k_full;
+        for (int32_t j = max(0, last_j - kTcStages + 1); j <= last_j; ++j)
+            mbar_wait_timeout(&full[j % kTcStages], static_cast<uint32_t>(j / kTcStages) & 1u);
     }
-    if (warp == 1 && lane == 0) mbar_wait_timeout(idle, 0);
+    if (warp == 1 && lane == 0) mbar_wait_timeout(idle, 0);  // any thread may wait on the barrier
     umma::fence_before_sync();
     __syncthreads();
     if (warp == 1) {
