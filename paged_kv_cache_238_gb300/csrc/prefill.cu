@@ -77,6 +77,29 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// Packed fp32 pairs (sm_100 family): one instruction for two lanes' worth of the softmax's
+// scale-and-shift and running sums, and a three-input maximum.
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b, float c) {
+    uint64_t a, bb, cc, d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(bb) : "f"(b));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(cc) : "f"(c));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(bb), "l"(cc));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(d));
+}
+__device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1) {
+    uint64_t a, d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(d0), "f"(d1));
+    asm("add.rn.f32x2 %0, %0, %1;" : "+l"(d) : "l"(a));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(d));
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 template <int G>
 __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -329,12 +352,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
                 umma::wait_ld();
                 if (!diag) {
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) mxk[i & 7] = fmaxf(mxk[i & 7], __uint_as_float(raw[i >> 5][i & 31]));
+                    for (int i = 0; i < 64; i += 2)
+                        mxk[(i >> 1) & 7] = max3(mxk[(i >> 1) & 7], __uint_as_float(raw[i >> 5][i & 31]),
+                                                 __uint_as_float(raw[i >> 5][(i + 1) & 31]));
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) {
-                        const float x = kbase + c2 * 64 + i > pos ? -INFINITY : __uint_as_float(raw[i >> 5][i & 31]);
-                        mxk[i & 7] = fmaxf(mxk[i & 7], x);
+                    for (int i = 0; i < 64; i += 2) {
+                        const float x0 = kbase + c2 * 64 + i > pos ? -INFINITY : __uint_as_float(raw[i >> 5][i & 31]);
+                        const float x1 =
+                            kbase + c2 * 64 + i + 1 > pos ? -INFINITY : __uint_as_float(raw[i >> 5][(i + 1) & 31]);
+                        mxk[(i >> 1) & 7] = max3(mxk[(i >> 1) & 7], x0, x1);
                     }
                 }
             }
@@ -347,32 +374,32 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
             const float m_new = grow ? fmaxf(m_ref, mx) : m_ref;
             const float alpha = first ? 0.f : fast_exp2(m_ref - m_new);
             const float neg_m = -m_new;
-            // pass 2: P = 2^(s scale - m) in bf16 pairs over the first 64 columns of S (each
-            // 64-key half is read before its 32 P columns are written)
-            float psk[8];
+            // pass 2: P = 2^(s scale - m) in bf16 pairs over the first 64 columns of S, 32 keys
+            // at a time (each group of S columns is read before the P columns that overwrite
+            // part of it are written)
+            float psk[8];  // four packed pairs of partial sums
 #pragma unroll
             for (int k = 0; k < 8; ++k) psk[k] = 0.f;
 #pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) {
-                uint32_t raw[2][32];
-                umma::ld_32x32b_x32(tmem_s + lane_off + c2 * 64, raw[0]);
-                umma::ld_32x32b_x32(tmem_s + lane_off + c2 * 64 + 32, raw[1]);
+            for (int c4 = 0; c4 < 4; ++c4) {
+                uint32_t raw[32];
+                umma::ld_32x32b_x32(tmem_s + lane_off + c4 * 32, raw);
                 umma::wait_ld();
                 if (diag) {  // masked keys: -inf, so their p is exactly 0
 #pragma unroll
-                    for (int i = 0; i < 64; ++i)
-                        if (kbase + c2 * 64 + i > pos) raw[i >> 5][i & 31] = __float_as_uint(-INFINITY);
+                    for (int i = 0; i < 32; ++i)
+                        if (kbase + c4 * 32 + i > pos) raw[i] = __float_as_uint(-INFINITY);
                 }
-                uint32_t pk[32];
+                uint32_t pk[16];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const float p0 = fast_exp2(fmaf(__uint_as_float(raw[e >> 4][(2 * e) & 31]), scale_log2, neg_m));
-                    const float p1 = fast_exp2(fmaf(__uint_as_float(raw[e >> 4][(2 * e + 1) & 31]), scale_log2, neg_m));
-                    psk[(2 * e) & 7] += p0;
-                    psk[(2 * e + 1) & 7] += p1;
+                for (int e = 0; e < 16; ++e) {
+                    float x0, x1;
+                    fma2(x0, x1, __uint_as_float(raw[2 * e]), __uint_as_float(raw[2 * e + 1]), scale_log2, neg_m);
+                    const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+                    add2(psk[2 * (e & 3)], psk[2 * (e & 3) + 1], p0, p1);
                     pk[e] = pack_bf16x2(p0, p1);
                 }
-                umma::st_32x32b_x32(tmem_s + lane_off + c2 * 32, pk);
+                umma::st_32x32b_x16(tmem_s + lane_off + c4 * 16, pk);
             }
             umma::wait_st();
             const float psum = ((psk[0] + psk[1]) + (psk[2] + psk[3])) + ((psk[4] + psk[5]) + (psk[6] + psk[7]));
