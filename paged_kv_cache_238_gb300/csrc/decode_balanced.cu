@@ -59,7 +59,7 @@ __host__ __device__ inline BalLayout bal_layout(int NW, int nst, uint32_t stage_
     L.ring = o;      o += static_cast<uint32_t>(NW) * nst * stage_bytes;
     L.piece0 = o;    o += static_cast<uint32_t>(NW) * G * D * 4u;             // each warp's first piece
     L.piece_ml = o;  o += static_cast<uint32_t>(NW) * 2u * G * 2u * 4u;       // (m, l) of both pieces
-    L.meta = o;      o += align_up(static_cast<uint32_t>(NW) * 2u * 4u, 16u);  // segment of each piece
+    L.meta = o;      o += align_up(static_cast<uint32_t>(NW) * 2u * 4u * 2u + 16u, 16u);  // pieces, group list
     L.bars = o;      o += static_cast<uint32_t>(NW) * nst * 8u;
     L.flags = o;     o += 16u;
     L.prefix = o;    o += align_up((S + 1) * 4u, 16u);
@@ -90,6 +90,14 @@ __host__ __device__ inline BalWorkspace bal_ws(void* base, int S, int Hkv, int G
     p += static_cast<size_t>(C) * 2 * G * D * 4;
     w.piece_ml = reinterpret_cast<float*>(p);
     return w;
+}
+
+// 2^x with the hardware approximation (relative error about 2^-22; 2^-inf = 0; results below
+// 2^-126 flush to 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 // First unit of slice c when U units are cut into C equal contiguous slices.
@@ -205,13 +213,13 @@ __device__ __forceinline__ void merge_pieces(__nv_bfloat16* o, int32_t a, int32_
                 float Mn = M[k];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) Mn = fmaxf(Mn, ml[j][k].x);
-                const float sc = (M[k] == -INFINITY) ? 0.f : exp2f(M[k] - Mn);
+                const float sc = (M[k] == -INFINITY) ? 0.f : fast_exp2(M[k] - Mn);
                 den[k] *= sc;
 #pragma unroll
                 for (int e = 0; e < E; ++e) acc[k][e] *= sc;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const float wj = (ml[j][k].x == -INFINITY) ? 0.f : ml[j][k].y * exp2f(ml[j][k].x - Mn);
+                    const float wj = (ml[j][k].x == -INFINITY) ? 0.f : ml[j][k].y * fast_exp2(ml[j][k].x - Mn);
                     den[k] += wj;
 #pragma unroll
                     for (int e = 0; e < E; ++e) acc[k][e] = fmaf(wj, v[j][k][e], acc[k][e]);
@@ -252,12 +260,15 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
     constexpr int NT = D / 8;   // n-tiles of the output row
     constexpr int E = D / 32;   // elements per lane in the merges
     constexpr int NTH = NW * 32;
+    static_assert(NW <= 8, "level-2 reductions cover the pieces of at most 8 warps");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const BalLayout L = bal_layout(NW, nst, stage_bytes, G, D, S);
     float* piece0 = reinterpret_cast<float*>(smem + L.piece0);
     float* piece_ml = reinterpret_cast<float*>(smem + L.piece_ml);
-    int32_t* meta = reinterpret_cast<int32_t*>(smem + L.meta);
+    int32_t* meta = reinterpret_cast<int32_t*>(smem + L.meta);  // [NW][2] segment of each piece
+    int32_t* glist = meta + 2 * NW;                                  // [2 NW] groups to merge (owner slot)
+    int32_t* gcount = glist + 2 * NW;                                // [2] crossing / internal group counts
     uint64_t* bars_all = reinterpret_cast<uint64_t*>(smem + L.bars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L.flags);
     int32_t* prefix = reinterpret_cast<int32_t*>(smem + L.prefix);
@@ -295,6 +306,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
         if (lane == 0) {
             meta[warp * 2] = -1;
             meta[warp * 2 + 1] = -1;
+            if (warp == 0) gcount[0] = gcount[1] = 0;
             for (int i = 0; i < nst; ++i) mbar_init(&bars_all[warp * nst + i], 1);
         }
         if (tid == 0) *abort_flag = 0;
@@ -482,16 +494,16 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
             const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-            const float c0 = exp2f(m0 - mn0), c1 = exp2f(m1 - mn1);
+            const float c0 = fast_exp2(m0 - mn0), c1 = fast_exp2(m1 - mn1);
             m0 = mn0;
             m1 = mn1;
             float ps[2][4];
 #pragma unroll
             for (int x = 0; x < 2; ++x) {
-                ps[x][0] = exp2f(sc[x][0] - mn0);
-                ps[x][1] = exp2f(sc[x][1] - mn0);
-                ps[x][2] = exp2f(sc[x][2] - mn1);
-                ps[x][3] = exp2f(sc[x][3] - mn1);
+                ps[x][0] = fast_exp2(sc[x][0] - mn0);
+                ps[x][1] = fast_exp2(sc[x][1] - mn0);
+                ps[x][2] = fast_exp2(sc[x][2] - mn1);
+                ps[x][3] = fast_exp2(sc[x][3] - mn1);
             }
             l0 = l0 * c0 + ps[0][0] + ps[0][1] + ps[1][0] + ps[1][1];
             l1 = l1 * c1 + ps[0][2] + ps[0][3] + ps[1][2] + ps[1][3];
@@ -588,31 +600,47 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
     if (*abort_flag) return;
 
     // ---- level 2: merge the pieces of segments cut between this CTA's warps ----------------
-    // A group is the run of pieces of one segment over consecutive warps: a warp's last piece
-    // (slot 1) always starts one (that segment began inside the warp); its first piece (slot 0)
-    // starts one only if no earlier warp of the CTA holds that segment. Each warp merges the
-    // groups that start at its own slots; lane i holds the group's i-th piece.
+    // A group is the run of pieces of one segment over consecutive warps of the CTA, named by
+    // the slot of its last piece; lane i of the warp that merges it holds the group's i-th
+    // piece counted from the end.
     auto warp_len = [&](int32_t w2) {
         return static_cast<int32_t>((static_cast<int64_t>(w2 + 1) * n_cta) / NW -
                                     (static_cast<int64_t>(w2) * n_cta) / NW);
     };
-    for (int32_t s0 = 0; s0 < 2; ++s0) {
-        const int32_t seg = meta[warp * 2 + s0];
-        if (seg < 0) continue;
-        if (s0 == 0) {  // does an earlier warp (skipping empty ones) hold this segment?
-            int32_t w2 = warp - 1;
-            while (w2 >= 0 && warp_len(w2) == 0) --w2;
-            if (w2 >= 0 && (meta[w2 * 2] == seg || meta[w2 * 2 + 1] == seg)) continue;
+    // List the groups by their owner slot: those cut by the CTA range too (they go on to the
+    // workspace merge, level 3) first, from the front, the others from the back; then the warps
+    // share them out, so two expensive groups rarely land on one warp.
+    if (lane == 0) {
+        for (int32_t s0 = 0; s0 < 2; ++s0) {
+            const int32_t seg = meta[warp * 2 + s0];
+            if (seg < 0) continue;
+            int32_t nxt = warp + 1;  // next warp of the CTA with units
+            while (nxt < NW && warp_len(nxt) == 0) ++nxt;
+            if (nxt < NW && meta[nxt * 2] == seg) continue;  // the group goes on in a later warp
+            const int32_t sq = seg / num_kv_heads, hq = seg - sq * num_kv_heads;
+            const int32_t npq = (prefix[sq + 1] - prefix[sq]) / num_kv_heads;
+            const int32_t sa = prefix[sq] + hq * npq;
+            const bool crossing = sa < u0 || sa + npq > u1;
+            if (crossing) glist[atomicAdd(&gcount[0], 1)] = warp * 2 + s0;
+            else glist[2 * NW - 1 - atomicAdd(&gcount[1], 1)] = warp * 2 + s0;
         }
-        int32_t my_slot = lane == 0 ? warp * 2 + s0 : -1;
+    }
+    __syncthreads();
+    const int32_t n_cross = gcount[0], n_groups = gcount[0] + gcount[1];
+    for (int32_t gi = warp; gi < n_groups; gi += NW) {
+        const int32_t owner = glist[gi < n_cross ? gi : 2 * NW - 1 - (gi - n_cross)];
+        const int32_t ow = owner >> 1, s0 = owner & 1;
+        const int32_t seg = meta[owner];
+        int32_t my_slot = lane == 0 ? owner : -1;
         int32_t nm = 1;
-        if (!(s0 == 0 && meta[warp * 2 + 1] >= 0)) {  // the segment runs past this warp
-            for (int32_t w2 = warp + 1; w2 < NW; ++w2) {
+        if (s0 == 0) {  // the segment may have begun in earlier warps
+            for (int32_t w2 = ow - 1; w2 >= 0; --w2) {
                 if (warp_len(w2) == 0) continue;
-                if (meta[w2 * 2] != seg) break;
-                if (lane == nm) my_slot = w2 * 2;
+                const int32_t slot2 = meta[w2 * 2 + 1] == seg ? w2 * 2 + 1 : (meta[w2 * 2] == seg ? w2 * 2 : -1);
+                if (slot2 < 0) break;
+                if (lane == nm) my_slot = slot2;
                 ++nm;
-                if (meta[w2 * 2 + 1] >= 0) break;  // the segment ends inside warp w2
+                if (slot2 & 1) break;  // the segment begins inside warp w2
             }
         }
         const int32_t s = seg / num_kv_heads, h = seg - s * num_kv_heads;
@@ -638,16 +666,16 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
 #pragma unroll
             for (int k = 0; k < 4; ++k) Mk[k] = mk[k];
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
+            for (int off = 4; off > 0; off >>= 1)  // a group has at most NW <= 8 pieces, in lanes 0..7
 #pragma unroll
                 for (int k = 0; k < 4; ++k) Mk[k] = fmaxf(Mk[k], __shfl_xor_sync(0xffffffffu, Mk[k], off));
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                wk[k] = my_slot >= 0 ? exp2f(mk[k] - Mk[k]) : 0.f;
+                wk[k] = my_slot >= 0 ? fast_exp2(mk[k] - Mk[k]) : 0.f;
                 dk[k] = lk[k] * wk[k];
             }
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
+            for (int off = 4; off > 0; off >>= 1)
 #pragma unroll
                 for (int k = 0; k < 4; ++k) dk[k] += __shfl_xor_sync(0xffffffffu, dk[k], off);
 #pragma unroll
