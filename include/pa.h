@@ -63,7 +63,9 @@ typedef enum {
     PA_OK = 0,
     PA_ERR_INVALID_ARG = 1,   /* a host-checkable argument is wrong; nothing launched  */
     PA_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. head_dim 96)           */
-    PA_ERR_CUDA = 3           /* a CUDA runtime call or launch failed                   */
+    PA_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed                   */
+    PA_ERR_NO_SPACE = 4       /* block manager: not enough free blocks (nothing changed),
+                                 or an output array too small for the answer            */
 } pa_status;
 
 typedef enum {
@@ -203,6 +205,97 @@ PA_API pa_status pa_get_device_errors(uint32_t* errors, int32_t clear);
 
 /* pa_status_string: static, human-readable name of a status code. */
 PA_API const char* pa_status_string(pa_status status);
+
+/*
+ * ==========================================================================================
+ * Block manager (host side): which physical blocks each request owns
+ * ==========================================================================================
+ * Host memory only, no device calls; one manager per KV pool; not thread-safe (one caller at
+ * a time). It produces the block-table rows and slot mappings the kernels above read.
+ *
+ * Model ("vLLM: what PagedAttention turned into", "The block pool, and the two tricks in it"
+ * and "What a block hash actually is"; "vLLM Internals", section 1.2):
+ *   - Block 0 is taken at construction as the null block and never handed out.
+ *   - Free blocks sit in one eviction-ordered queue; new blocks come from its front. A freed
+ *     block without a hash goes to the front (reused first), one with a hash to the back
+ *     (evicted last). A request's blocks are freed tail first.
+ *   - A freed block keeps its hash and can still be hit; it leaves the cache only when it is
+ *     taken for new content.
+ *   - Block hash: SHA-256(parent hash || the block's 16 token ids as int32 little-endian ||
+ *     extra key), chained from SHA-256(hash_seed); the extra key is the request's salt, on
+ *     the first block only; the cache key is hash || group id 0 (4 bytes, big-endian).
+ *   - A new request reuses the longest run of cached full blocks of its prompt (stopping at
+ *     the first miss), at most (n_tokens - 1) / 16 of them, so at least one token is left to
+ *     compute.
+ *   - Blocks are reference counted. pa_bm_fork makes a request that shares every block of its
+ *     parent (parallel sampling stores the prompt once); appending into a shared, partly
+ *     filled last block first moves the request to a private copy, whose (source,
+ *     destination) pair waits in the manager until pa_bm_take_copies hands it to
+ *     pa_copy_blocks, which must run before the request's next K/V write.
+ *   - A full block is entered into the cache once pa_bm_commit reports its K/V computed.
+ * Calls that fail return a status and change nothing.
+ */
+typedef struct pa_block_manager pa_block_manager;
+
+/* A manager for a pool of num_blocks (>= 2) blocks; enable_caching 0 disables prefix reuse;
+ * hash_seed NULL = "paged-kv-none-hash". Free with pa_bm_destroy. */
+PA_API pa_status pa_bm_create(int32_t num_blocks, int32_t enable_caching, const char* hash_seed,
+                              pa_block_manager** out);
+PA_API void pa_bm_destroy(pa_block_manager* bm);
+/* Blocks in the free queue (cached-but-free blocks included); -1 for a NULL manager. */
+PA_API int32_t pa_bm_num_free_blocks(const pa_block_manager* bm);
+
+/* A new request with its prompt tokens (host int32[n_tokens], n_tokens >= 1) and optional
+ * salt bytes; allocates ceil(n_tokens / 16) blocks, the cached prefix ones shared;
+ * *num_cached_tokens = tokens whose K/V is already in the pool (a multiple of 16).
+ * PA_ERR_INVALID_ARG for a known req_id; PA_ERR_NO_SPACE when the pool is short. */
+PA_API pa_status pa_bm_add_request(pa_block_manager* bm, int64_t req_id, const int32_t* tokens, int32_t n_tokens,
+                                   const uint8_t* salt, int32_t salt_len, int32_t* num_cached_tokens);
+/* Appends n tokens (e.g. one per decode step), allocating blocks at block boundaries and
+ * copying a shared, partly filled last block first (copy-on-write). */
+PA_API pa_status pa_bm_append_tokens(pa_block_manager* bm, int64_t req_id, const int32_t* tokens, int32_t n);
+/* The first num_computed_tokens tokens of the request have their K/V in the pool: its full
+ * blocks among them are hashed and entered into the prefix cache. */
+PA_API pa_status pa_bm_commit(pa_block_manager* bm, int64_t req_id, int32_t num_computed_tokens);
+/* child_id shares every block (and the tokens) of parent_id. */
+PA_API pa_status pa_bm_fork(pa_block_manager* bm, int64_t parent_id, int64_t child_id);
+/* Releases the request's blocks, tail first. */
+PA_API pa_status pa_bm_free_request(pa_block_manager* bm, int64_t req_id);
+
+/* The request's block-table row: block_ids[i] for i < capacity, padded with the null block;
+ * *num_blocks = blocks the request holds (PA_ERR_NO_SPACE if more than capacity). */
+PA_API pa_status pa_bm_get_blocks(const pa_block_manager* bm, int64_t req_id, int32_t* block_ids, int32_t capacity,
+                                  int32_t* num_blocks);
+/* Slots (block * 16 + offset) of positions first_pos .. first_pos + n - 1 of the request,
+ * which must lie inside its blocks. */
+PA_API pa_status pa_bm_slot_mapping(const pa_block_manager* bm, int64_t req_id, int32_t first_pos, int32_t n,
+                                    int64_t* slots);
+/* Moves up to capacity pending copy-on-write pairs (oldest first) into src / dst;
+ * PA_ERR_NO_SPACE if some remain. */
+PA_API pa_status pa_bm_take_copies(pa_block_manager* bm, int32_t* src, int32_t* dst, int32_t capacity,
+                                   int32_t* n_copies);
+/* Inspection: the free queue from front to back, and one block's reference count and hash. */
+PA_API pa_status pa_bm_free_queue(const pa_block_manager* bm, int32_t* order, int32_t capacity, int32_t* n);
+PA_API pa_status pa_bm_block_info(const pa_block_manager* bm, int32_t block_id, int32_t* ref_count,
+                                  uint8_t* hash32, int32_t* has_hash);
+/* Pool size for a memory budget: floor(utilization * free_bytes / per-block bytes over all
+ * layers, K and V) ("vLLM: what PagedAttention turned into", "Checking the 96.3%": the pool
+ * is sized once from a utilisation fraction of free memory); -1 on a bad argument. */
+PA_API int64_t pa_bm_num_blocks_for_memory(size_t free_bytes, double utilization, int32_t num_layers,
+                                           int32_t num_kv_heads, int32_t head_dim, pa_dtype dtype);
+/* SHA-256 (FIPS 180-4) of n bytes, as the block hashes use it. */
+PA_API pa_status pa_sha256(const uint8_t* data, size_t n, uint8_t* out32);
+
+/*
+ * pa_copy_blocks: for each of the n_pairs (src, dst) block-id pairs in block_pairs (device
+ * int32 [n_pairs][2]), copy block src of k_cache and of v_cache, every kv head, into block
+ * dst (the copy-on-write pairs of the block manager). Pairs must not chain (no dst is another
+ * pair's src); src == dst is skipped. Out-of-range ids are not copied and set
+ * PA_DEVERR_BLOCK_RANGE. Asynchronous on `stream`.
+ */
+PA_API pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_pairs, int32_t n_pairs,
+                                int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, pa_dtype dtype,
+                                void* stream);
 
 #ifdef __cplusplus
 }

@@ -171,6 +171,11 @@ class BlockPool:
 
     def append_tokens(self, rid: int, tokens: List[int]) -> None:
         r = self.reqs[rid]
+        pos0 = len(r.tokens)
+        need = sum(1 for p in range(pos0, pos0 + len(tokens)) if p % BLOCK == 0)
+        cow = len(tokens) > 0 and pos0 % BLOCK != 0 and self.blocks[r.blocks[-1]].ref > 1
+        if need + int(cow) > len(self.queue):
+            raise MemoryError("out of blocks")  # nothing changed
         for t in tokens:
             pos = len(r.tokens)
             if pos % BLOCK == 0:

@@ -33,7 +33,7 @@ def nvcc_path() -> str:
 
 
 def _sources():
-    cu = sorted(f for f in os.listdir(CSRC) if f.endswith(".cu"))
+    cu = sorted(f for f in os.listdir(CSRC) if f.endswith((".cu", ".cpp")))
     deps = sorted(f for f in os.listdir(CSRC) if f.endswith((".cuh", ".h")))
     return cu, deps
 
@@ -63,7 +63,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     cu, _ = _sources()
 
     def compile_one(name):
-        obj = os.path.join(BUILD, name[:-3] + ".o")
+        obj = os.path.join(BUILD, name.rsplit(".", 1)[0] + ".o")
         cmd = [nvcc] + NVCC_FLAGS + list(extra_flags) + ["-c", os.path.join(CSRC, name), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:

@@ -13,14 +13,18 @@ from typing import Optional
 
 from . import _build
 
-PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA = 0, 1, 2, 3
+PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_NO_SPACE = 0, 1, 2, 3, 4
 PA_F32, PA_BF16 = 0, 1
 PA_DEVERR_SLOT_RANGE, PA_DEVERR_BLOCK_RANGE, PA_DEVERR_LEN_RANGE, PA_DEVERR_WAIT_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 BLOCK_SIZE = 16
 
 #: every symbol that include/pa.h declares
 EXPORTED = ("pa_reshape_and_cache", "pa_decode_workspace_size", "pa_decode", "pa_prefill_chunk",
-            "pa_decode_noalloc", "pa_get_device_errors", "pa_status_string")
+            "pa_decode_noalloc", "pa_get_device_errors", "pa_status_string",
+            "pa_bm_create", "pa_bm_destroy", "pa_bm_num_free_blocks", "pa_bm_add_request", "pa_bm_append_tokens",
+            "pa_bm_commit", "pa_bm_fork", "pa_bm_free_request", "pa_bm_get_blocks", "pa_bm_slot_mapping",
+            "pa_bm_take_copies", "pa_bm_free_queue", "pa_bm_block_info", "pa_bm_num_blocks_for_memory", "pa_sha256",
+            "pa_copy_blocks")
 #: size of the library's fixed scratch used by pa_decode_noalloc
 PA_DECODE_NOALLOC_MAX_BYTES = 16 * 1024 * 1024
 
@@ -59,6 +63,28 @@ def load(build_if_needed: bool = True) -> ctypes.CDLL:
                                               ctypes.c_int, vp]
             lib.pa_get_device_errors.restype = ctypes.c_int
             lib.pa_get_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
+            i64, pi32, pi64, pu8 = (ctypes.c_int64, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64),
+                                    ctypes.POINTER(ctypes.c_uint8))
+            for name, res, args in (
+                    ("pa_bm_create", ctypes.c_int, [i32, i32, ctypes.c_char_p, ctypes.POINTER(vp)]),
+                    ("pa_bm_destroy", None, [vp]),
+                    ("pa_bm_num_free_blocks", i32, [vp]),
+                    ("pa_bm_add_request", ctypes.c_int, [vp, i64, pi32, i32, pu8, i32, pi32]),
+                    ("pa_bm_append_tokens", ctypes.c_int, [vp, i64, pi32, i32]),
+                    ("pa_bm_commit", ctypes.c_int, [vp, i64, i32]),
+                    ("pa_bm_fork", ctypes.c_int, [vp, i64, i64]),
+                    ("pa_bm_free_request", ctypes.c_int, [vp, i64]),
+                    ("pa_bm_get_blocks", ctypes.c_int, [vp, i64, pi32, i32, pi32]),
+                    ("pa_bm_slot_mapping", ctypes.c_int, [vp, i64, i32, i32, pi64]),
+                    ("pa_bm_take_copies", ctypes.c_int, [vp, pi32, pi32, i32, pi32]),
+                    ("pa_bm_free_queue", ctypes.c_int, [vp, pi32, i32, pi32]),
+                    ("pa_bm_block_info", ctypes.c_int, [vp, i32, pi32, pu8, pi32]),
+                    ("pa_bm_num_blocks_for_memory", i64, [sz, ctypes.c_double, i32, i32, i32, ctypes.c_int]),
+                    ("pa_sha256", ctypes.c_int, [vp, sz, pu8]),
+                    ("pa_copy_blocks", ctypes.c_int, [vp, vp, vp, i32, i32, i32, i32, ctypes.c_int, vp])):
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
             _lib = lib
     return _lib
 
@@ -164,3 +190,108 @@ def pa_get_device_errors(clear: bool = True) -> int:
     v = ctypes.c_uint32(0)
     _check("pa_get_device_errors", load().pa_get_device_errors(ctypes.byref(v), 1 if clear else 0))
     return int(v.value)
+
+
+def pa_copy_blocks(k_cache, v_cache, block_pairs, stream=None) -> None:
+    """k_cache, v_cache: [NB, H_kv, 16, D]; block_pairs: int32 CUDA tensor [n, 2] of (src, dst)."""
+    _need_cuda(k_cache, v_cache, block_pairs)
+    NB, H_kv, _, D = k_cache.shape
+    _check("pa_copy_blocks", load().pa_copy_blocks(
+        _ptr(k_cache), _ptr(v_cache), _ptr(block_pairs), block_pairs.shape[0], H_kv, D, NB, _dtype_code(k_cache),
+        _stream(stream)))
+
+
+def pa_sha256(data: bytes) -> bytes:
+    out = (ctypes.c_uint8 * 32)()
+    buf = (ctypes.c_uint8 * max(1, len(data))).from_buffer_copy(data or b"\0")
+    _check("pa_sha256", load().pa_sha256(ctypes.cast(buf, ctypes.c_void_p), len(data), out))
+    return bytes(out)
+
+
+def pa_bm_num_blocks_for_memory(free_bytes: int, utilization: float, num_layers: int, num_kv_heads: int,
+                                head_dim: int, dtype) -> int:
+    import torch
+    code = dtype if isinstance(dtype, int) else (PA_F32 if dtype == torch.float32 else PA_BF16)
+    return int(load().pa_bm_num_blocks_for_memory(free_bytes, utilization, num_layers, num_kv_heads, head_dim, code))
+
+
+def _i32(xs):
+    arr = (ctypes.c_int32 * max(1, len(xs)))(*xs)
+    return arr
+
+
+class BlockManager:
+    """The library's host block manager (pa_bm_* in include/pa.h), one per KV pool."""
+
+    def __init__(self, num_blocks: int, enable_caching: bool = True, hash_seed: Optional[str] = None):
+        h = ctypes.c_void_p()
+        _check("pa_bm_create", load().pa_bm_create(num_blocks, 1 if enable_caching else 0,
+                                                   None if hash_seed is None else hash_seed.encode(),
+                                                   ctypes.byref(h)))
+        self._h = h
+        self._lib = load()
+
+    def close(self) -> None:
+        if self._h:
+            self._lib.pa_bm_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def num_free(self) -> int:
+        return int(self._lib.pa_bm_num_free_blocks(self._h))
+
+    def add_request(self, req_id: int, tokens, salt: bytes = b"") -> int:
+        n = ctypes.c_int32(0)
+        sb = (ctypes.c_uint8 * max(1, len(salt))).from_buffer_copy(salt or b"\0")
+        _check("pa_bm_add_request", self._lib.pa_bm_add_request(self._h, req_id, _i32(list(tokens)), len(tokens), sb,
+                                                                len(salt), ctypes.byref(n)))
+        return int(n.value)
+
+    def append_tokens(self, req_id: int, tokens) -> None:
+        _check("pa_bm_append_tokens", self._lib.pa_bm_append_tokens(self._h, req_id, _i32(list(tokens)), len(tokens)))
+
+    def commit(self, req_id: int, num_computed: int) -> None:
+        _check("pa_bm_commit", self._lib.pa_bm_commit(self._h, req_id, num_computed))
+
+    def fork(self, parent: int, child: int) -> None:
+        _check("pa_bm_fork", self._lib.pa_bm_fork(self._h, parent, child))
+
+    def free_request(self, req_id: int) -> None:
+        _check("pa_bm_free_request", self._lib.pa_bm_free_request(self._h, req_id))
+
+    def block_ids(self, req_id: int, capacity: Optional[int] = None):
+        n = ctypes.c_int32(0)
+        self._lib.pa_bm_get_blocks(self._h, req_id, None, 0, ctypes.byref(n))
+        cap = n.value if capacity is None else capacity
+        buf = (ctypes.c_int32 * max(1, cap))()
+        st = self._lib.pa_bm_get_blocks(self._h, req_id, buf, cap, ctypes.byref(n))
+        if st not in (PA_OK, PA_ERR_NO_SPACE):
+            raise PaError("pa_bm_get_blocks", st)
+        return list(buf[:cap])
+
+    def slot_mapping(self, req_id: int, first: int, n: int):
+        buf = (ctypes.c_int64 * max(1, n))()
+        _check("pa_bm_slot_mapping", self._lib.pa_bm_slot_mapping(self._h, req_id, first, n, buf))
+        return list(buf[:n])
+
+    def take_copies(self, capacity: int = 4096):
+        src, dst, n = (ctypes.c_int32 * capacity)(), (ctypes.c_int32 * capacity)(), ctypes.c_int32(0)
+        _check("pa_bm_take_copies", self._lib.pa_bm_take_copies(self._h, src, dst, capacity, ctypes.byref(n)))
+        return [(src[i], dst[i]) for i in range(n.value)]
+
+    def free_queue(self):
+        cap = max(1, self.num_free())
+        buf, n = (ctypes.c_int32 * cap)(), ctypes.c_int32(0)
+        _check("pa_bm_free_queue", self._lib.pa_bm_free_queue(self._h, buf, cap, ctypes.byref(n)))
+        return list(buf[:n.value])
+
+    def block_info(self, block_id: int):
+        ref, has = ctypes.c_int32(0), ctypes.c_int32(0)
+        h = (ctypes.c_uint8 * 32)()
+        _check("pa_bm_block_info", self._lib.pa_bm_block_info(self._h, block_id, ctypes.byref(ref), h, ctypes.byref(has)))
+        return int(ref.value), (bytes(h) if has.value else None)

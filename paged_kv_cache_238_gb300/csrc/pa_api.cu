@@ -142,6 +142,7 @@ PA_API const char* pa_status_string(pa_status status) {
         case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
         case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
         case PA_ERR_CUDA: return "PA_ERR_CUDA";
+        case PA_ERR_NO_SPACE: return "PA_ERR_NO_SPACE";
     }
     return "PA_UNKNOWN_STATUS";
 }
@@ -166,6 +167,26 @@ PA_API pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_cach
     return launch_reshape_and_cache(a, dev->info.num_sms, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? PA_OK
                : PA_ERR_CUDA;
+}
+
+PA_API pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_pairs, int32_t n_pairs,
+                                int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, pa_dtype dtype,
+                                void* stream) {
+    if (n_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0) return PA_ERR_INVALID_ARG;
+    if (!dtype_ok(dtype)) return PA_ERR_INVALID_ARG;
+    if ((head_dim * elem_bytes(dtype)) % 16 != 0) return PA_ERR_UNSUPPORTED;
+    if (n_pairs == 0) return PA_OK;
+    if (n_pairs > 0x7fffffff / 2) return PA_ERR_UNSUPPORTED;
+    if (!k_cache || !v_cache || !block_pairs) return PA_ERR_INVALID_ARG;
+    if (!aligned16(k_cache) || !aligned16(v_cache) || (reinterpret_cast<uintptr_t>(block_pairs) & 3u))
+        return PA_ERR_INVALID_ARG;
+    const int64_t chunks = static_cast<int64_t>(num_kv_heads) * 16 * head_dim * elem_bytes(dtype) / 16;
+    if (chunks > 0x7fffffffLL || (chunks + 255) / 256 > 65535) return PA_ERR_UNSUPPORTED;
+    DeviceCache* dev = nullptr;
+    if (device_cache(&dev) != cudaSuccess) return PA_ERR_CUDA;
+    CopyBlocksArgs a{k_cache, v_cache, block_pairs, n_pairs, num_kv_heads, head_dim, num_blocks, elem_bytes(dtype),
+                     dev->err};
+    return launch_copy_blocks(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 PA_API size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,

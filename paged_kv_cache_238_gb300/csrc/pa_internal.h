@@ -26,6 +26,18 @@ struct ReshapeArgs {
 cudaError_t launch_reshape_and_cache(const ReshapeArgs& a, int num_sms, cudaStream_t stream);
 
 // ------------------------------------------------------------------------------------------
+// copy_blocks (copy-on-write pairs of the block manager)
+// ------------------------------------------------------------------------------------------
+struct CopyBlocksArgs {
+    void* k_cache;
+    void* v_cache;
+    const int32_t* pairs;  // device [num_pairs][2] (src, dst)
+    int32_t num_pairs, num_kv_heads, head_dim, num_blocks, elem_bytes;
+    uint32_t* err;
+};
+cudaError_t launch_copy_blocks(const CopyBlocksArgs& a, cudaStream_t stream);
+
+// ------------------------------------------------------------------------------------------
 // decode
 // ------------------------------------------------------------------------------------------
 struct DecodeArgs {
