@@ -15,10 +15,12 @@
 // (128-byte swizzle; at head_dim 128 a 3-D box of 64 columns x 16 rows x 2 column halves, so the
 // page lands as two 2 KB swizzled halves) completing on the stage's mbarrier; when the unit starts
 // a new segment it also bulk-copies that segment's G query rows into the stage. Block ids are
-// fetched 32 units ahead by the warp's lanes. The warp consumes a stage (S = Q K^T and
-// O += P V on mma.sync m16n8k16 with the G q heads that share a kv head as rows, so each page
-// is read once for the whole group; online softmax in registers, log2 domain) and refills it
-// with the unit `stages` ahead. The unused tail of a sequence's last block may hold anything:
+// fetched 32 units ahead by the warp's lanes. The warp consumes a stage and refills it with
+// the unit `stages` ahead. The math runs transposed on mma.sync m16n8k16 so that the page's 16
+// keys fill the 16 rows: S^T = K Q^T (the G q heads that share the kv head as the 8 or 16
+// columns, so each page is read once for the whole group), then O^T += V^T P^T with P^T
+// brought into the B-operand layout by a register transpose (movmatrix); online softmax in
+// registers, log2 domain. The unused tail of a sequence's last block may hold anything:
 // its keys are masked to -inf and its V rows zeroed in shared memory before P V.
 //
 // Split-KV reduce, in three levels, all with the same log-sum-exp merge
@@ -248,7 +250,7 @@ __device__ __forceinline__ int32_t count_piece(int32_t* counter) {
     return old;
 }
 
-template <int D, int NW>
+template <int D, int NW, int NH>  // NH: groups of 8 q heads (G <= 8 * NH)
 __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
     __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ block_table,
@@ -257,7 +259,6 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
     constexpr uint32_t kPage = kBlock * D * 2;
     constexpr uint32_t kHalves = D / 64;
     constexpr int KS = D / 16;  // k-steps over head_dim
-    constexpr int NT = D / 8;   // n-tiles of the output row
     constexpr int E = D / 32;   // elements per lane in the merges
     constexpr int NTH = NW * 32;
     static_assert(NW <= 8, "level-2 reductions cover the pieces of at most 8 warps");
@@ -407,9 +408,15 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
 
         Walker wc;
         wc.at(prefix, lens, S, num_kv_heads, a_w);
-        uint32_t qa[KS][4];
-        float acc[NT][4];
-        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+        constexpr int NMT = D / 16;  // m-tiles of O^T (16 head_dim rows each)
+        // Fragment ownership (gid = lane / 4, tig = lane % 4):
+        //   qb[nh][ks]   Q^T as B: head 8 nh + gid, dims 16 ks + 2 tig (+1) and + 8
+        //   sc[nh][e]    S^T: key gid + 8 (e / 2), head 8 nh + 2 tig + e % 2
+        //   acc[nh][mt]  O^T: head_dim 16 mt + gid + 8 (e / 2), head 8 nh + 2 tig + e % 2
+        //   mh, lh       running max and partial sum of heads 8 nh + 2 tig + {0, 1}
+        uint32_t qb[NH][KS][2];
+        float acc[NH][NMT][4];
+        float mh[NH][2], lh[NH][2];
         int32_t t_first = 0;
 
         for (int32_t t = 0; t < n; ++t) {
@@ -431,19 +438,21 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
             if (seg_first) {
                 // the segment's G query rows were copied into this stage with the page
                 const __nv_bfloat16* qs = reinterpret_cast<const __nv_bfloat16*>(stage + 2u * kPage);
-                const bool r0 = gid < G, r1 = gid + 8 < G;
 #pragma unroll
-                for (int ks = 0; ks < KS; ++ks) {
-                    const int c0 = ks * 16 + tig * 2;
-                    qa[ks][0] = r0 ? *reinterpret_cast<const uint32_t*>(qs + gid * D + c0) : 0u;
-                    qa[ks][1] = r1 ? *reinterpret_cast<const uint32_t*>(qs + (gid + 8) * D + c0) : 0u;
-                    qa[ks][2] = r0 ? *reinterpret_cast<const uint32_t*>(qs + gid * D + c0 + 8) : 0u;
-                    qa[ks][3] = r1 ? *reinterpret_cast<const uint32_t*>(qs + (gid + 8) * D + c0 + 8) : 0u;
+                for (int nh = 0; nh < NH; ++nh) {
+                    const int32_t head = nh * 8 + gid;
+                    const bool valid = head < G;
+#pragma unroll
+                    for (int ks = 0; ks < KS; ++ks) {
+                        const int c0 = ks * 16 + tig * 2;
+                        qb[nh][ks][0] = valid ? *reinterpret_cast<const uint32_t*>(qs + head * D + c0) : 0u;
+                        qb[nh][ks][1] = valid ? *reinterpret_cast<const uint32_t*>(qs + head * D + c0 + 8) : 0u;
+                    }
+#pragma unroll
+                    for (int mt = 0; mt < NMT; ++mt) acc[nh][mt][0] = acc[nh][mt][1] = acc[nh][mt][2] = acc[nh][mt][3] = 0.f;
+                    mh[nh][0] = mh[nh][1] = -INFINITY;
+                    lh[nh][0] = lh[nh][1] = 0.f;
                 }
-#pragma unroll
-                for (int nn = 0; nn < NT; ++nn) acc[nn][0] = acc[nn][1] = acc[nn][2] = acc[nn][3] = 0.f;
-                m0 = m1 = -INFINITY;
-                l0 = l1 = 0.f;
                 t_first = t;
             }
             const int32_t ntok = min(kBlock, wc.len - wc.j * kBlock);
@@ -458,131 +467,135 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
                 __syncwarp();
             }
 
-            // S = Q K^T : rows = q heads (G of 16 valid), columns = the page's 16 tokens
-            float sc[2][4];
+            // S^T = K Q^T: rows = the page's 16 keys, columns = q heads
+            const uint32_t mat = lane >> 3, r8 = lane & 7;
+            float sc[NH][4];
 #pragma unroll
-            for (int x = 0; x < 2; ++x) sc[x][0] = sc[x][1] = sc[x][2] = sc[x][3] = 0.f;
-            {
-                const uint32_t mat = lane >> 3, r = lane & 7;
+            for (int nh = 0; nh < NH; ++nh) sc[nh][0] = sc[nh][1] = sc[nh][2] = sc[nh][3] = 0.f;
 #pragma unroll
-                for (int p = 0; p < KS / 2; ++p) {
+            for (int ks = 0; ks < KS; ++ks) {
+                // A fragments: matrix mat = (keys 8 (mat % 2) .., 16-byte chunk 2 ks + mat / 2)
+                const uint32_t key = r8 + 8u * (mat & 1u), chunk = ks * 2 + (mat >> 1);
+                uint32_t a[4];
+                ldsm_x4(k_u32 + (chunk >> 3) * 2048u + sw128_offset(key, chunk & 7u), a[0], a[1], a[2], a[3]);
 #pragma unroll
-                    for (int x = 0; x < 2; ++x) {
-                        const uint32_t chunk = p * 4 + mat;
-                        const uint32_t addr = k_u32 + (chunk >> 3) * 2048u + sw128_offset(x * 8 + r, chunk & 7u);
-                        uint32_t b0, b1, b2, b3;
-                        ldsm_x4(addr, b0, b1, b2, b3);
-                        mma_16816(sc[x], qa[2 * p], b0, b1);
-                        mma_16816(sc[x], qa[2 * p + 1], b2, b3);
-                    }
-                }
+                for (int nh = 0; nh < NH; ++nh) mma_16816(sc[nh], a, qb[nh][ks][0], qb[nh][ks][1]);
             }
-            // online softmax in the log2 domain; sc[x][e] is token 8x + 2 tig + (e & 1)
-            float mx0 = -INFINITY, mx1 = -INFINITY;
+            // online softmax per head (column) in the log2 domain: reduce over the 16 keys =
+            // the two rows a thread holds and the 8 lanes with the same tig
+            float mx[NH][2];
 #pragma unroll
-            for (int x = 0; x < 2; ++x) {
+            for (int nh = 0; nh < NH; ++nh) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int token = x * 8 + tig * 2 + (e & 1);
-                    const float v = token < ntok ? sc[x][e] * scale_log2 : -INFINITY;
-                    sc[x][e] = v;
-                    if (e < 2) mx0 = fmaxf(mx0, v); else mx1 = fmaxf(mx1, v);
+                    const int32_t k_in = gid + 8 * (e >> 1);
+                    sc[nh][e] = k_in < ntok ? sc[nh][e] * scale_log2 : -INFINITY;
                 }
+                mx[nh][0] = fmaxf(sc[nh][0], sc[nh][2]);
+                mx[nh][1] = fmaxf(sc[nh][1], sc[nh][3]);
             }
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-            const float c0 = fast_exp2(m0 - mn0), c1 = fast_exp2(m1 - mn1);
-            m0 = mn0;
-            m1 = mn1;
-            float ps[2][4];
 #pragma unroll
-            for (int x = 0; x < 2; ++x) {
-                ps[x][0] = fast_exp2(sc[x][0] - mn0);
-                ps[x][1] = fast_exp2(sc[x][1] - mn0);
-                ps[x][2] = fast_exp2(sc[x][2] - mn1);
-                ps[x][3] = fast_exp2(sc[x][3] - mn1);
-            }
-            l0 = l0 * c0 + ps[0][0] + ps[0][1] + ps[1][0] + ps[1][1];
-            l1 = l1 * c1 + ps[0][2] + ps[0][3] + ps[1][2] + ps[1][3];
+            for (int off = 4; off < 32; off <<= 1)
 #pragma unroll
-            for (int nn = 0; nn < NT; ++nn) {
-                acc[nn][0] *= c0;
-                acc[nn][1] *= c0;
-                acc[nn][2] *= c1;
-                acc[nn][3] *= c1;
-            }
-            uint32_t pa[4];
-            pa[0] = pack_bf16x2(ps[0][0], ps[0][1]);
-            pa[1] = pack_bf16x2(ps[0][2], ps[0][3]);
-            pa[2] = pack_bf16x2(ps[1][0], ps[1][1]);
-            pa[3] = pack_bf16x2(ps[1][2], ps[1][3]);
-            // O += P V
-            {
-                const uint32_t mat = lane >> 3, r = lane & 7;
-                const uint32_t token = (mat & 1u) * 8 + r;
-#pragma unroll
-                for (int p = 0; p < NT / 2; ++p) {
-                    const uint32_t chunk = p * 2 + (mat >> 1);
-                    const uint32_t addr = v_u32 + (chunk >> 3) * 2048u + sw128_offset(token, chunk & 7u);
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_trans(addr, b0, b1, b2, b3);
-                    mma_16816(acc[2 * p], pa, b0, b1);
-                    mma_16816(acc[2 * p + 1], pa, b2, b3);
+                for (int nh = 0; nh < NH; ++nh) {
+                    mx[nh][0] = fmaxf(mx[nh][0], __shfl_xor_sync(0xffffffffu, mx[nh][0], off));
+                    mx[nh][1] = fmaxf(mx[nh][1], __shfl_xor_sync(0xffffffffu, mx[nh][1], off));
                 }
+            uint32_t pb[NH][2];
+#pragma unroll
+            for (int nh = 0; nh < NH; ++nh) {
+                float cc[2];
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const float mn = fmaxf(mh[nh][hh], mx[nh][hh]);
+                    cc[hh] = fast_exp2(mh[nh][hh] - mn);
+                    mh[nh][hh] = mn;
+                }
+                float p[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) p[e] = fast_exp2(sc[nh][e] - mh[nh][e & 1]);
+                lh[nh][0] = lh[nh][0] * cc[0] + p[0] + p[2];
+                lh[nh][1] = lh[nh][1] * cc[1] + p[1] + p[3];
+#pragma unroll
+                for (int mt = 0; mt < NMT; ++mt) {
+                    acc[nh][mt][0] *= cc[0];
+                    acc[nh][mt][1] *= cc[1];
+                    acc[nh][mt][2] *= cc[0];
+                    acc[nh][mt][3] *= cc[1];
+                }
+                // P^T as the B operand of O^T += V^T P^T: transpose the two 8 x 8 (key, head)
+                // blocks held in the accumulator layout
+                pb[nh][0] = movmatrix_trans(pack_bf16x2(p[0], p[1]));
+                pb[nh][1] = movmatrix_trans(pack_bf16x2(p[2], p[3]));
+            }
+            // O^T += V^T P^T: rows = head_dim (16 per m-tile), columns = q heads, k = keys
+#pragma unroll
+            for (int mt = 0; mt < NMT; ++mt) {
+                // A fragments (transposed loads): matrix mat = (keys 8 (mat / 2) .., chunk 2 mt + mat % 2)
+                const uint32_t key = r8 + 8u * (mat >> 1), chunk = mt * 2 + (mat & 1u);
+                uint32_t a[4];
+                ldsm_x4_trans(v_u32 + (chunk >> 3) * 2048u + sw128_offset(key, chunk & 7u), a[0], a[1], a[2], a[3]);
+#pragma unroll
+                for (int nh = 0; nh < NH; ++nh) mma_16816(acc[nh][mt], a, pb[nh][0], pb[nh][1]);
             }
 
             const bool seg_last = (t == n - 1) || (wc.j == wc.np - 1);
             if (seg_last) {
-                float L0 = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
-                L0 += __shfl_xor_sync(0xffffffffu, L0, 2);
-                float L1 = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
-                L1 += __shfl_xor_sync(0xffffffffu, L1, 2);
+                float Lh[NH][2];
+#pragma unroll
+                for (int nh = 0; nh < NH; ++nh) {
+                    Lh[nh][0] = lh[nh][0];
+                    Lh[nh][1] = lh[nh][1];
+                }
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1)
+#pragma unroll
+                    for (int nh = 0; nh < NH; ++nh) {
+                        Lh[nh][0] += __shfl_xor_sync(0xffffffffu, Lh[nh][0], off);
+                        Lh[nh][1] += __shfl_xor_sync(0xffffffffu, Lh[nh][1], off);
+                    }
                 const int32_t seg_a = prefix[wc.s] + wc.h * wc.np, seg_b = seg_a + wc.np;
                 if (seg_a >= a_w && seg_b <= b_w) {
                     // whole segment inside this warp: normalise and write out
                     __nv_bfloat16* o = out + (static_cast<int64_t>(wc.s) * Hq + wc.h * G) * D;
-                    const float i0 = 1.f / L0, i1 = 1.f / L1;
-                    if (gid < G) {
 #pragma unroll
-                        for (int nn = 0; nn < NT; ++nn)
-                            *reinterpret_cast<uint32_t*>(o + gid * D + nn * 8 + tig * 2) =
-                                pack_bf16x2(acc[nn][0] * i0, acc[nn][1] * i0);
-                    }
-                    if (gid + 8 < G) {
+                    for (int nh = 0; nh < NH; ++nh)
 #pragma unroll
-                        for (int nn = 0; nn < NT; ++nn)
-                            *reinterpret_cast<uint32_t*>(o + (gid + 8) * D + nn * 8 + tig * 2) =
-                                pack_bf16x2(acc[nn][2] * i1, acc[nn][3] * i1);
-                    }
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int32_t head = nh * 8 + tig * 2 + hh;
+                            if (head >= G) continue;
+                            const float inv = 1.f / Lh[nh][hh];
+                            __nv_bfloat16* orow = o + head * D + gid;
+#pragma unroll
+                            for (int mt = 0; mt < NMT; ++mt) {
+                                orow[mt * 16] = __float2bfloat16_rn(acc[nh][mt][hh] * inv);
+                                orow[mt * 16 + 8] = __float2bfloat16_rn(acc[nh][mt][2 + hh] * inv);
+                            }
+                        }
                 } else {
                     // piece of a segment cut by the warp's sub-slice, kept for the CTA merge:
                     // slot 0 = the sub-slice's first segment (own buffer), slot 1 = its last
-                    // one, finalised after the last unit, when the warp's ring is idle
+                    // one, finalised with the last unit, when the warp's ring is idle
                     const int slot = (t_first == 0) ? 0 : 1;
                     __syncwarp();
                     float* pa_acc = slot == 0 ? piece0 + static_cast<uint32_t>(warp) * G * D
                                               : reinterpret_cast<float*>(ring);
-                    if (gid < G) {
 #pragma unroll
-                        for (int nn = 0; nn < NT; ++nn)
-                            *reinterpret_cast<float2*>(pa_acc + gid * D + nn * 8 + tig * 2) =
-                                make_float2(acc[nn][0], acc[nn][1]);
-                        if (tig == 0)
-                            *reinterpret_cast<float2*>(piece_ml + ((warp * 2 + slot) * G + gid) * 2) =
-                                make_float2(m0, L0);
-                    }
-                    if (gid + 8 < G) {
+                    for (int nh = 0; nh < NH; ++nh)
 #pragma unroll
-                        for (int nn = 0; nn < NT; ++nn)
-                            *reinterpret_cast<float2*>(pa_acc + (gid + 8) * D + nn * 8 + tig * 2) =
-                                make_float2(acc[nn][2], acc[nn][3]);
-                        if (tig == 0)
-                            *reinterpret_cast<float2*>(piece_ml + ((warp * 2 + slot) * G + gid + 8) * 2) =
-                                make_float2(m1, L1);
-                    }
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int32_t head = nh * 8 + tig * 2 + hh;
+                            if (head >= G) continue;
+                            float* prow = pa_acc + head * D + gid;
+#pragma unroll
+                            for (int mt = 0; mt < NMT; ++mt) {
+                                prow[mt * 16] = acc[nh][mt][hh];
+                                prow[mt * 16 + 8] = acc[nh][mt][2 + hh];
+                            }
+                            if (gid == 0)
+                                *reinterpret_cast<float2*>(piece_ml + ((warp * 2 + slot) * G + head) * 2) =
+                                    make_float2(mh[nh][hh], Lh[nh][hh]);
+                        }
                     if (lane == 0) meta[warp * 2 + slot] = wc.s * num_kv_heads + wc.h;
                 }
             }
@@ -743,7 +756,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
     }
 }
 
-template <int D, int NW>
+template <int D, int NW, int NH>
 cudaError_t launch_impl(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream) {
     alignas(64) CUtensorMap tm_k, tm_v;
     const uint64_t rows = static_cast<uint64_t>(a.num_blocks) * a.num_kv_heads * kBlock;
@@ -761,7 +774,7 @@ cudaError_t launch_impl(const DecodeArgs& a, const DecodePlan& plan, cudaStream_
     }
     if (e != cudaSuccess) return e;
     const int32_t G = a.num_q_heads / a.num_kv_heads;
-    e = cudaFuncSetAttribute(decode_balanced_kernel<D, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(decode_balanced_kernel<D, NW, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(plan.smem_bytes));
     if (e != cudaSuccess) return e;
     BalWorkspace ws = bal_ws(a.workspace, a.num_seqs, a.num_kv_heads, G, D, plan.num_ctas);
@@ -778,7 +791,7 @@ cudaError_t launch_impl(const DecodeArgs& a, const DecodePlan& plan, cudaStream_
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_balanced_kernel<D, NW>, tm_k, tm_v, static_cast<__nv_bfloat16*>(a.out),
+    return cudaLaunchKernelEx(&cfg, decode_balanced_kernel<D, NW, NH>, tm_k, tm_v, static_cast<__nv_bfloat16*>(a.out),
                               static_cast<const __nv_bfloat16*>(a.q), a.block_table, a.max_blocks_per_seq,
                               a.seq_lens, a.num_seqs, a.num_kv_heads, G, a.num_blocks, a.scale * kLog2e, plan.stages,
                               plan.stage_bytes, ws, a.err);
@@ -787,10 +800,10 @@ cudaError_t launch_impl(const DecodeArgs& a, const DecodePlan& plan, cudaStream_
 template <int D, int NW>
 int ctas_per_sm(uint32_t smem) {
     int n = 0;
-    if (cudaFuncSetAttribute(decode_balanced_kernel<D, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(decode_balanced_kernel<D, NW, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
         return 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_balanced_kernel<D, NW>, NW * 32, smem) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_balanced_kernel<D, NW, 2>, NW * 32, smem) !=
         cudaSuccess)
         return 0;
     return n;
@@ -823,9 +836,13 @@ bool plan_decode_balanced(int32_t S, int32_t Hkv, int32_t G, int32_t D, const De
 }
 
 cudaError_t launch_decode_balanced(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream) {
-    if (a.head_dim == 128)
-        return plan.warps == 8 ? launch_impl<128, 8>(a, plan, stream) : launch_impl<128, 4>(a, plan, stream);
-    return plan.warps == 8 ? launch_impl<64, 8>(a, plan, stream) : launch_impl<64, 4>(a, plan, stream);
+    const bool wide = a.num_q_heads / a.num_kv_heads > 8;  // 9..16 q heads per kv head
+    if (a.head_dim == 128) {
+        if (plan.warps == 8) return wide ? launch_impl<128, 8, 2>(a, plan, stream) : launch_impl<128, 8, 1>(a, plan, stream);
+        return wide ? launch_impl<128, 4, 2>(a, plan, stream) : launch_impl<128, 4, 1>(a, plan, stream);
+    }
+    if (plan.warps == 8) return wide ? launch_impl<64, 8, 2>(a, plan, stream) : launch_impl<64, 8, 1>(a, plan, stream);
+    return wide ? launch_impl<64, 4, 2>(a, plan, stream) : launch_impl<64, 4, 1>(a, plan, stream);
 }
 
 }  // namespace pa
