@@ -57,10 +57,10 @@ def build(force: bool = False) -> str:
 def _declare(lib):
     vp, i32 = ctypes.c_void_p, ctypes.c_int32
     lib.oracle_reshape_and_cache.restype = ctypes.c_int
-    lib.oracle_reshape_and_cache.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32]
+    lib.oracle_reshape_and_cache.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32]
     lib.oracle_attention.restype = ctypes.c_int
     lib.oracle_attention.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32,
-                                     i32, i32, i32, i32, ctypes.c_double, i32, i32]
+                                     i32, i32, i32, i32, i32, ctypes.c_double, i32, i32]
     return lib
 
 
@@ -90,10 +90,11 @@ def _c(a, dtype=None):
 
 
 def reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, _lib_override=None) -> None:
-    """In-place: k_cache[s // 16, :, s % 16, :] = k[t] (same for v), for s = slot_mapping[t] >= 0.
+    """In-place: k_cache[s // bs, :, s % bs, :] = k[t] (same for v), for s = slot_mapping[t] >= 0.
 
-    k, v: [T, H_kv, D]; k_cache, v_cache: [num_blocks, H_kv, 16, D] (C-contiguous,
-    modified in place); slot_mapping: [T] int64.
+    k, v: [T, H_kv, D]; k_cache, v_cache: [num_blocks, H_kv, bs, D] (C-contiguous,
+    modified in place; the block size bs is the pool's third dimension, 16 by default);
+    slot_mapping: [T] int64.
     """
     k = _c(k)
     v = _c(v)
@@ -102,10 +103,11 @@ def reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, _lib_override=None) 
     assert k.dtype == v.dtype == k_cache.dtype == v_cache.dtype
     T, H_kv, D = k.shape
     nb = k_cache.shape[0]
-    assert k_cache.shape == (nb, H_kv, BLOCK_SIZE, D) and v_cache.shape == k_cache.shape
+    bs = k_cache.shape[2]
+    assert k_cache.shape == (nb, H_kv, bs, D) and v_cache.shape == k_cache.shape
     assert slots.shape == (T,)
     rc = (_lib_override or _load()).oracle_reshape_and_cache(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(slots),
-                                          T, H_kv, D, nb, k.dtype.itemsize)
+                                          T, H_kv, D, nb, bs, k.dtype.itemsize)
     if rc != 0:
         raise ValueError("oracle_reshape_and_cache: slot outside the pool")
 
@@ -114,7 +116,8 @@ def attention(q, k_cache, v_cache, block_table, seq_lens, scale, query_start_loc
               num_threads: int = 0, _lib_override=None) -> np.ndarray:
     """Exact fp64 paged attention. Returns float64 [T_q, H_q, D].
 
-    q: [T_q, H_q, D] (T_q = S for decode); k_cache, v_cache: [NB, H_kv, 16, D];
+    q: [T_q, H_q, D] (T_q = S for decode); k_cache, v_cache: [NB, H_kv, bs, D] (bs, the
+    block size, is the pool's third dimension);
     block_table: [S, max_blocks] int32; seq_lens: [S] int32 (keys incl. the current
     token); query_start_loc: None (decode) or [S + 1] int32 prefix sums of chunk lengths.
     num_threads: OpenMP threads (0 = runtime default).
@@ -128,7 +131,7 @@ def attention(q, k_cache, v_cache, block_table, seq_lens, scale, query_start_loc
     assert q.dtype == k_cache.dtype == v_cache.dtype
     T_q, H_q, D = q.shape
     nb, H_kv, bs, D2 = k_cache.shape
-    assert bs == BLOCK_SIZE and D2 == D and v_cache.shape == k_cache.shape
+    assert bs > 0 and D2 == D and v_cache.shape == k_cache.shape
     S = lens.shape[0]
     if bt.ndim != 2 or bt.shape[0] != S:
         raise ValueError("block_table must be [S, max_blocks]")
@@ -142,7 +145,7 @@ def attention(q, k_cache, v_cache, block_table, seq_lens, scale, query_start_loc
         qsl_ptr = _ptr(qsl)
     out = np.empty((T_q, H_q, D), dtype=np.float64)
     rc = (_lib_override or _load()).oracle_attention(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(bt), bt.shape[1],
-                                  _ptr(lens), qsl_ptr, S, H_q, H_kv, D, nb, float(scale), dt,
+                                  _ptr(lens), qsl_ptr, S, H_q, H_kv, D, nb, bs, float(scale), dt,
                                   int(num_threads))
     if rc != 0:
         raise ValueError("oracle_attention: invalid tables (block id, length or chunk out of range)")

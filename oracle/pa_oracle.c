@@ -11,8 +11,10 @@
  *    ("vLLM Internals", section 1.1; "My Understanding of vLLM and
  *    PagedAttention", sections "Logical Blocks", "Physical Blocks",
  *    "Block Table").
- *  - The block size is 16 tokens ("vLLM: what PagedAttention turned into",
- *    intro table and "The problem PagedAttention was actually solving").
+ *  - The block size is 16 tokens by default ("vLLM: what PagedAttention turned
+ *    into", intro table and "The problem PagedAttention was actually solving");
+ *    the same page reports that sizes from 16 to 128 perform alike, so the block
+ *    size is an argument (bs below).
  *  - A slot is an int64 index into the pool, one per new token, used to write
  *    new K/V ("vLLM: what PagedAttention turned into", same section: the int64
  *    slot_mapping mirrored to the device).
@@ -22,9 +24,9 @@
  *    so the exact result is softmax(scale * q K^T) V over the visible keys.
  *
  * Readings taken where the pages are silent:
- *  - Pool layout: separate K and V arrays, each [num_blocks][H_kv][16][D].
- *  - slot = physical_block * 16 + offset; positions are 0-based, so position p
- *    lives in logical block p / 16 at offset p % 16.
+ *  - Pool layout: separate K and V arrays, each [num_blocks][H_kv][bs][D].
+ *  - slot = physical_block * bs + offset; positions are 0-based, so position p
+ *    lives in logical block p / bs at offset p % bs.
  *  - A negative slot means "no write" (the token is skipped).
  *  - GQA: query head h reads kv head h / (H_q / H_kv).
  *  - seq_len counts every key of the sequence, including the current token.
@@ -46,7 +48,6 @@
 #include <omp.h>
 #endif
 
-#define ORACLE_BLOCK_SIZE 16
 
 enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
 enum { ORACLE_OK = 0, ORACLE_ERR = 1 };
@@ -65,23 +66,26 @@ static double load_elem(const void* base, size_t i, int dtype) {
 
 /*
  * Write the K/V rows of T new tokens into their slots. Token t goes to
- * physical block slot[t] / 16 at in-block offset slot[t] % 16, for every kv
- * head. The copy is bitwise in the stored element type (elem_bytes 4 or 2).
+ * physical block slot[t] / bs at in-block offset slot[t] % bs (bs = block_size,
+ * 16 by default; "vLLM: what PagedAttention turned into" gives 16 and says
+ * 16-128 perform alike), for every kv head. The copy is bitwise in the stored
+ * element type (elem_bytes 4 or 2).
  * Returns ORACLE_ERR (and writes nothing more) on a slot beyond the pool.
  */
 int oracle_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
                              const int64_t* slot_mapping, int32_t T, int32_t H_kv, int32_t D,
-                             int32_t num_blocks, int32_t elem_bytes) {
+                             int32_t num_blocks, int32_t block_size, int32_t elem_bytes) {
     const size_t row = (size_t)D * (size_t)elem_bytes;
+    if (block_size <= 0) return ORACLE_ERR;
     for (int32_t t = 0; t < T; ++t) {
         int64_t slot = slot_mapping[t];
         if (slot < 0) continue;
-        int64_t block = slot / ORACLE_BLOCK_SIZE;
-        int64_t offset = slot % ORACLE_BLOCK_SIZE;
+        int64_t block = slot / block_size;
+        int64_t offset = slot % block_size;
         if (block >= num_blocks) return ORACLE_ERR;
         for (int32_t h = 0; h < H_kv; ++h) {
             size_t src = ((size_t)t * H_kv + h) * row;
-            size_t dst = (((size_t)block * H_kv + h) * ORACLE_BLOCK_SIZE + (size_t)offset) * row;
+            size_t dst = (((size_t)block * H_kv + h) * (size_t)block_size + (size_t)offset) * row;
             memcpy((char*)k_cache + dst, (const char*)k + src, row);
             memcpy((char*)v_cache + dst, (const char*)v + src, row);
         }
@@ -94,7 +98,7 @@ int oracle_reshape_and_cache(const void* k, const void* v, void* k_cache, void* 
  *
  * out            [T_q][H_q][D] fp64, T_q = S (decode) or query_start_loc[S] (prefill)
  * q              [T_q][H_q][D] in the stored dtype
- * k_cache/v_cache [num_blocks][H_kv][16][D] in the stored dtype
+ * k_cache/v_cache [num_blocks][H_kv][block_size][D] in the stored dtype
  * block_table    [S][max_blocks_per_seq] int32
  * seq_lens       [S] total keys per sequence, current token(s) included
  * query_start_loc NULL for decode (one query row per sequence, at position
@@ -103,16 +107,16 @@ int oracle_reshape_and_cache(const void* k, const void* v, void* k_cache, void* 
 int oracle_attention(double* out, const void* q, const void* k_cache, const void* v_cache,
                      const int32_t* block_table, int32_t max_blocks_per_seq,
                      const int32_t* seq_lens, const int32_t* query_start_loc, int32_t S,
-                     int32_t H_q, int32_t H_kv, int32_t D, int32_t num_blocks, double scale,
-                     int32_t dtype, int32_t num_threads) {
-    if (S < 0 || H_q <= 0 || H_kv <= 0 || D <= 0 || H_q % H_kv != 0) return ORACLE_ERR;
+                     int32_t H_q, int32_t H_kv, int32_t D, int32_t num_blocks, int32_t block_size,
+                     double scale, int32_t dtype, int32_t num_threads) {
+    if (S < 0 || H_q <= 0 || H_kv <= 0 || D <= 0 || H_q % H_kv != 0 || block_size <= 0) return ORACLE_ERR;
     const int32_t group = H_q / H_kv;
 
     /* Validate the tables first so the parallel loop below cannot fail. */
     for (int32_t i = 0; i < S; ++i) {
         int32_t len = seq_lens[i];
         if (len < 0) return ORACLE_ERR;
-        int32_t n_blocks = (len + ORACLE_BLOCK_SIZE - 1) / ORACLE_BLOCK_SIZE;
+        int32_t n_blocks = (len + block_size - 1) / block_size;
         if (n_blocks > max_blocks_per_seq) return ORACLE_ERR;
         for (int32_t j = 0; j < n_blocks; ++j) {
             int32_t phys = block_table[(size_t)i * max_blocks_per_seq + j];
@@ -144,7 +148,7 @@ int oracle_attention(double* out, const void* q, const void* k_cache, const void
         }
 
         /* Gather: logical token j of kv head g comes from physical block
-         * block_table[i][j / 16] at offset j % 16. */
+         * block_table[i][j / bs] at offset j % bs. */
         double* K = (double*)malloc(sizeof(double) * (size_t)H_kv * len * D);
         double* V = (double*)malloc(sizeof(double) * (size_t)H_kv * len * D);
         double* z = (double*)malloc(sizeof(double) * (size_t)len);
@@ -156,8 +160,8 @@ int oracle_attention(double* out, const void* q, const void* k_cache, const void
         }
         for (int32_t g = 0; g < H_kv; ++g) {
             for (int32_t j = 0; j < len; ++j) {
-                int32_t phys = block_table[(size_t)i * max_blocks_per_seq + j / ORACLE_BLOCK_SIZE];
-                size_t src = (((size_t)phys * H_kv + g) * ORACLE_BLOCK_SIZE + (size_t)(j % ORACLE_BLOCK_SIZE)) * D;
+                int32_t phys = block_table[(size_t)i * max_blocks_per_seq + j / block_size];
+                size_t src = (((size_t)phys * H_kv + g) * (size_t)block_size + (size_t)(j % block_size)) * D;
                 size_t dst = ((size_t)g * len + j) * D;
                 for (int32_t d = 0; d < D; ++d) {
                     K[dst + d] = load_elem(k_cache, src + d, dtype);

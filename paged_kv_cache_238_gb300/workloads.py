@@ -79,7 +79,7 @@ class Workload:
     D: int
     num_blocks: int
     scale: float
-    k_cache: np.ndarray             # [NB, H_kv, 16, D]
+    k_cache: np.ndarray             # [NB, H_kv, block_size, D]
     v_cache: np.ndarray
     # decode part
     q: Optional[np.ndarray] = None              # [S, H_q, D]
@@ -133,12 +133,13 @@ def _table(ids_per_seq: List[np.ndarray], max_blocks: Optional[int] = None) -> n
 
 def _store_tokens(pool: np.ndarray, ids: np.ndarray, first: int, vals: np.ndarray) -> None:
     """Place vals[j] (j = 0..n-1, [n, H_kv, D]) at logical positions first..first+n-1 of a
-    sequence whose logical blocks are ``ids``."""
+    sequence whose logical blocks are ``ids`` (block size = the pool's third dimension)."""
     n = vals.shape[0]
     if n == 0:
         return
+    bs = pool.shape[2]
     pos = np.arange(first, first + n)
-    pool[ids[pos // BLOCK], :, pos % BLOCK, :] = vals
+    pool[ids[pos // bs], :, pos % bs, :] = vals
 
 
 # --------------------------------------------------------------------------------------
@@ -147,10 +148,12 @@ def _store_tokens(pool: np.ndarray, ids: np.ndarray, first: int, vals: np.ndarra
 
 def build_decode(seed: int, lens, H_q: int, H_kv: int, D: int, num_blocks: int, dtype: str,
                  new_token: bool = True, shared_prefix_tokens: int = 0, keep_contiguous: bool = False,
-                 name: str = "decode", max_blocks: Optional[int] = None, poison: bool = True) -> Workload:
+                 name: str = "decode", max_blocks: Optional[int] = None, poison: bool = True,
+                 block_size: int = BLOCK) -> Workload:
     """Decode batch: one query per sequence at position len-1.
 
-    shared_prefix_tokens: if > 0 (a multiple of 16), every sequence's first
+    block_size: tokens per physical block (16 by default; 32, 64, 128 are the variants).
+    shared_prefix_tokens: if > 0 (a multiple of the block size), every sequence's first
     shared_prefix_tokens keys alias the same physical blocks (same values).
     new_token: key len-1 of each sequence arrives through reshape_and_cache
     (its pool cell starts poisoned) instead of being in the pool already.
@@ -158,16 +161,17 @@ def build_decode(seed: int, lens, H_q: int, H_kv: int, D: int, num_blocks: int, 
     rng = np.random.default_rng(seed)
     lens = np.asarray(lens, dtype=np.int64)
     S = lens.shape[0]
-    if shared_prefix_tokens % BLOCK:
+    BS = int(block_size)
+    if shared_prefix_tokens % BS:
         raise ValueError("shared prefix must be block aligned")
     if new_token and shared_prefix_tokens and np.any(lens <= shared_prefix_tokens):
         raise ValueError("a new token may not land in a shared block")
     alloc = _BlockAllocator(rng, num_blocks)
-    pool_shape = (num_blocks, H_kv, BLOCK, D)
+    pool_shape = (num_blocks, H_kv, BS, D)
     k_cache = _nan_like_pool(pool_shape, dtype) if poison else np.zeros(pool_shape, _np_dtype(dtype))
     v_cache = _nan_like_pool(pool_shape, dtype) if poison else np.zeros(pool_shape, _np_dtype(dtype))
 
-    n_shared_blocks = shared_prefix_tokens // BLOCK
+    n_shared_blocks = shared_prefix_tokens // BS
     shared_ids = alloc.take(n_shared_blocks)
     shared_k = _draw(rng, (shared_prefix_tokens, H_kv, D), dtype)
     shared_v = _draw(rng, (shared_prefix_tokens, H_kv, D), dtype)
@@ -180,7 +184,7 @@ def build_decode(seed: int, lens, H_q: int, H_kv: int, D: int, num_blocks: int, 
     slots = np.empty((S,), dtype=np.int64)
     for i in range(S):
         L = int(lens[i])
-        nblk = (L + BLOCK - 1) // BLOCK
+        nblk = (L + BS - 1) // BS
         own = alloc.take(max(0, nblk - n_shared_blocks))
         ids = np.concatenate([shared_ids[:min(nblk, n_shared_blocks)], own]).astype(np.int64)
         ids_per_seq.append(ids)
@@ -193,7 +197,7 @@ def build_decode(seed: int, lens, H_q: int, H_kv: int, D: int, num_blocks: int, 
         if new_token and L > 0:
             k_new[i] = kk[-1]
             v_new[i] = vv[-1]
-            slots[i] = int(ids[(L - 1) // BLOCK]) * BLOCK + (L - 1) % BLOCK
+            slots[i] = int(ids[(L - 1) // BS]) * BS + (L - 1) % BS
         else:
             k_new[i] = 0
             v_new[i] = 0
@@ -220,17 +224,18 @@ def _np_dtype(dtype: str):
 
 def build_mixed(seed: int, prior_lens, chunk_lens, decode_lens, H_q: int, H_kv: int, D: int,
                 num_blocks: int, dtype: str = "bf16", pad_multiple: int = 256,
-                keep_contiguous: bool = False, name: str = "mixed") -> Workload:
+                keep_contiguous: bool = False, name: str = "mixed", block_size: int = BLOCK) -> Workload:
     """Mixed step: chunked-prefill sequences (prior context in the pool, a chunk of new
     tokens written by reshape_and_cache) plus decode sequences (one new token each).
     The new-token list is padded to a multiple of ``pad_multiple`` with padding slots
-    that point into the null block 0 (slot i % 16)."""
+    that point into the null block 0 (slot i % block_size)."""
+    BS = int(block_size)
     rng = np.random.default_rng(seed)
     prior_lens = np.asarray(prior_lens, dtype=np.int64)
     chunk_lens = np.asarray(chunk_lens, dtype=np.int64)
     decode_lens = np.asarray(decode_lens, dtype=np.int64)
     alloc = _BlockAllocator(rng, num_blocks)
-    pool_shape = (num_blocks, H_kv, BLOCK, D)
+    pool_shape = (num_blocks, H_kv, BS, D)
     k_cache = _nan_like_pool(pool_shape, dtype)
     v_cache = _nan_like_pool(pool_shape, dtype)
 
@@ -239,7 +244,7 @@ def build_mixed(seed: int, prior_lens, chunk_lens, decode_lens, H_q: int, H_kv: 
     for i in range(prior_lens.shape[0]):
         P, C = int(prior_lens[i]), int(chunk_lens[i])
         L = P + C
-        ids = alloc.take((L + BLOCK - 1) // BLOCK)
+        ids = alloc.take((L + BS - 1) // BS)
         ids_p.append(ids)
         kk = _draw(rng, (L, H_kv, D), dtype)
         vv = _draw(rng, (L, H_kv, D), dtype)
@@ -248,14 +253,14 @@ def build_mixed(seed: int, prior_lens, chunk_lens, decode_lens, H_q: int, H_kv: 
         pos = np.arange(P, L)
         new_k.append(kk[P:])
         new_v.append(vv[P:])
-        new_slots.append(ids[pos // BLOCK] * BLOCK + pos % BLOCK)
+        new_slots.append(ids[pos // BS] * BS + pos % BS)
         if keep_contiguous:
             ck_p.append(kk)
             cv_p.append(vv)
     ids_d, ck_d, cv_d = [], [], []
     for i in range(decode_lens.shape[0]):
         L = int(decode_lens[i])
-        ids = alloc.take((L + BLOCK - 1) // BLOCK)
+        ids = alloc.take((L + BS - 1) // BS)
         ids_d.append(ids)
         kk = _draw(rng, (L, H_kv, D), dtype)
         vv = _draw(rng, (L, H_kv, D), dtype)
@@ -263,7 +268,7 @@ def build_mixed(seed: int, prior_lens, chunk_lens, decode_lens, H_q: int, H_kv: 
         _store_tokens(v_cache, ids, 0, vv[:L - 1])
         new_k.append(kk[L - 1:])
         new_v.append(vv[L - 1:])
-        new_slots.append(np.array([ids[(L - 1) // BLOCK] * BLOCK + (L - 1) % BLOCK], dtype=np.int64))
+        new_slots.append(np.array([ids[(L - 1) // BS] * BS + (L - 1) % BS], dtype=np.int64))
         if keep_contiguous:
             ck_d.append(kk)
             cv_d.append(vv)
@@ -276,7 +281,7 @@ def build_mixed(seed: int, prior_lens, chunk_lens, decode_lens, H_q: int, H_kv: 
         n_pad = T_pad - T
         k_new = np.concatenate([k_new, _draw(rng, (n_pad, H_kv, D), dtype)], axis=0)
         v_new = np.concatenate([v_new, _draw(rng, (n_pad, H_kv, D), dtype)], axis=0)
-        slots = np.concatenate([slots, np.arange(n_pad, dtype=np.int64) % BLOCK])  # block 0
+        slots = np.concatenate([slots, np.arange(n_pad, dtype=np.int64) % BS])  # block 0
     q_p = _draw(rng, (int(chunk_lens.sum()), H_q, D), dtype)
     q_d = _draw(rng, (decode_lens.shape[0], H_q, D), dtype)
     qsl = np.zeros((chunk_lens.shape[0] + 1,), dtype=np.int32)

@@ -21,12 +21,16 @@ MUTANTS = [
     ("causal_one_short", "const int32_t pos = len - chunk + r;",
      "const int32_t pos = (len - chunk + r > 0) ? len - chunk + r - 1 : 0;"),
     ("top_left_causal", "const int32_t pos = len - chunk + r;", "const int32_t pos = (chunk > 1) ? r : len - 1;"),
-    ("gather_offset", "(size_t)(j % ORACLE_BLOCK_SIZE)) * D;", "(size_t)((j + 1) % ORACLE_BLOCK_SIZE)) * D;"),
-    ("gather_head_stride", "size_t src = (((size_t)phys * H_kv + g) * ORACLE_BLOCK_SIZE",
-     "size_t src = (((size_t)phys * H_kv + (H_kv - 1 - g)) * ORACLE_BLOCK_SIZE"),
+    ("gather_offset", "(size_t)(j % block_size)) * D;", "(size_t)((j + 1) % block_size)) * D;"),
+    ("gather_head_stride", "size_t src = (((size_t)phys * H_kv + g) * (size_t)block_size",
+     "size_t src = (((size_t)phys * H_kv + (H_kv - 1 - g)) * (size_t)block_size"),
     ("pool_layout_swapped",
-     "size_t dst = (((size_t)block * H_kv + h) * ORACLE_BLOCK_SIZE + (size_t)offset) * row;",
-     "size_t dst = (((size_t)block * ORACLE_BLOCK_SIZE + (size_t)offset) * H_kv + h) * row;"),
+     "size_t dst = (((size_t)block * H_kv + h) * (size_t)block_size + (size_t)offset) * row;",
+     "size_t dst = (((size_t)block * (size_t)block_size + (size_t)offset) * H_kv + h) * row;"),
+    ("gather_block_size_fixed_16",
+     "int32_t phys = block_table[(size_t)i * max_blocks_per_seq + j / block_size];",
+     "int32_t phys = block_table[(size_t)i * max_blocks_per_seq + j / 16];"),
+    ("reshape_block_size_fixed_16", "int64_t offset = slot % block_size;", "int64_t offset = slot % 16;"),
     ("bf16_widening", "<< 16;", "<< 15;"),
     ("negative_slot_written", "if (slot < 0) continue;", "if (slot < 0) slot = 0;"),
 ]
@@ -81,7 +85,22 @@ def _pins(lib):
                                  np.array([-1, 17], np.int64), _lib_override=lib)
         assert (kc[0] == 9.0).all() and (kc[1, 0, 1] == 1.0).all()
 
+    def block_size_32_bruteforce():
+        # 32-token blocks: the same brute force over a pool whose third dimension is 32
+        wl = W.build_decode(35, [40, 64, 9], H_q=4, H_kv=2, D=8, num_blocks=12, dtype="f32",
+                            keep_contiguous=True, block_size=32)
+        kc, vc = wl.k_cache.copy(), wl.v_cache.copy()
+        oracle.reshape_and_cache(wl.k_new, wl.v_new, kc, vc, wl.slot_mapping, _lib_override=lib)
+        out = oracle.attention(wl.q, kc, vc, wl.block_table, wl.seq_lens, wl.scale, _lib_override=lib)
+        for i in range(wl.S):
+            K, V = W.as_f64(wl.contiguous_k[i]), W.as_f64(wl.contiguous_v[i])
+            for h in range(wl.H_q):
+                z = wl.scale * K[:, h // 2] @ W.as_f64(wl.q[i, h])
+                p = np.exp(z - z.max())
+                np.testing.assert_allclose(out[i, h], (p / p.sum()) @ V[:, h // 2], rtol=1e-10, atol=1e-10)
+
     check("bf16_gqa_bruteforce", bf16_gqa_bruteforce)
+    check("block_size_32_bruteforce", block_size_32_bruteforce)
     check("prefill_sdpa", prefill_sdpa)
     check("reshape_negative_slot_skipped", reshape_negative_slot_skipped)
     return failed
@@ -100,7 +119,7 @@ def _build_variant(tmp_path, text, repl, tag):
 
 @pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
 def test_unmutated_copy_passes_every_pin(tmp_path):
-    lib = _build_variant(tmp_path, "#define ORACLE_BLOCK_SIZE 16", "#define ORACLE_BLOCK_SIZE 16", "identity")
+    lib = _build_variant(tmp_path, "#include <math.h>", "#include <math.h>", "identity")
     assert _pins(lib) == []
 
 

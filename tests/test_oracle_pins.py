@@ -312,3 +312,80 @@ def test_lognormal_mix_has_the_length_implied_by_963_percent():
     wl = W.gqa_decode()
     assert abs(float(wl.seq_lens.mean()) - L) / L < 0.05
     assert wl.seq_lens.min() >= 16 and wl.seq_lens.max() <= 2048
+
+
+# ----------------------------------------------------------------------------- block-size variants
+
+@pytest.mark.parametrize("bs", [32, 64, 128])
+def test_decode_matches_bruteforce_for_larger_blocks(bs):
+    # "vLLM: what PagedAttention turned into": block sizes 16 to 128 all work; the result is
+    # still plain attention over the sequence's keys in logical order
+    wl = W.build_decode(40 + bs, [1, bs - 1, bs, bs + 1, 3 * bs + 5], H_q=8, H_kv=2, D=16,
+                        num_blocks=24, dtype="bf16", keep_contiguous=True, block_size=bs)
+    assert wl.k_cache.shape[2] == bs
+    kc, vc = _full_pool(wl)
+    out = oracle.attention(wl.q, kc, vc, wl.block_table, wl.seq_lens, wl.scale)
+    ref = brute_decode(wl.q, wl.contiguous_k, wl.contiguous_v, wl.scale, wl.H_kv)
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+
+
+def _repack(kc, bt, lens, bs_new):
+    """Move each sequence's keys, in logical order, into fresh blocks of size bs_new."""
+    NB, H, bs, D = kc.shape
+    per = [-(-int(L) // bs_new) for L in lens]
+    out = np.zeros((1 + sum(per), H, bs_new, D), kc.dtype)
+    bt2 = np.zeros((len(lens), max(per + [1])), np.int32)
+    nxt = 1
+    for i, L in enumerate(lens):
+        for p in range(int(L)):
+            if p % bs_new == 0:
+                bt2[i, p // bs_new] = nxt
+                nxt += 1
+            out[bt2[i, p // bs_new], :, p % bs_new] = kc[bt[i, p // bs], :, p % bs]
+    return out, bt2
+
+
+@pytest.mark.parametrize("bs", [32, 128])
+def test_reblocking_is_bit_identical(bs):
+    """The same keys stored in 16-token blocks or in bs-token blocks give the same bits:
+    the block size only changes where a key sits."""
+    wl = W.build_decode(50 + bs, [7, 200, 129, 64], H_q=4, H_kv=2, D=8, num_blocks=16,
+                        dtype="bf16", block_size=bs)
+    kc, vc = _full_pool(wl)
+    base = oracle.attention(wl.q, kc, vc, wl.block_table, wl.seq_lens, wl.scale)
+    k16, bt16 = _repack(kc, wl.block_table, wl.seq_lens, 16)
+    v16, _ = _repack(vc, wl.block_table, wl.seq_lens, 16)
+    assert k16.shape[2] == 16
+    out = oracle.attention(wl.q, k16, v16, bt16, wl.seq_lens, wl.scale)
+    assert np.array_equal(base, out)
+
+
+def test_reshape_with_64_token_blocks_places_slot_s_at_block_s_div_64():
+    rng = np.random.default_rng(60)
+    kc = np.zeros((4, 2, 64, 8), np.float32)
+    vc = kc.copy()
+    k = rng.standard_normal((3, 2, 8)).astype(np.float32)
+    v = rng.standard_normal((3, 2, 8)).astype(np.float32)
+    oracle.reshape_and_cache(k, v, kc, vc, np.array([0, 63, 64 * 3 + 17], np.int64))
+    assert np.array_equal(kc[0, :, 0], k[0]) and np.array_equal(kc[0, :, 63], k[1])
+    assert np.array_equal(kc[3, :, 17], k[2]) and np.array_equal(vc[3, :, 17], v[2])
+    assert np.count_nonzero(kc) == 3 * 2 * 8
+
+
+def test_prefill_with_64_token_blocks_matches_torch_sdpa():
+    torch = pytest.importorskip("torch")
+    wl = W.build_mixed(61, prior_lens=[0, 70], chunk_lens=[65, 30], decode_lens=[5], H_q=4, H_kv=2,
+                       D=16, num_blocks=16, dtype="f32", pad_multiple=0, keep_contiguous=True,
+                       block_size=64)
+    kc, vc = _full_pool(wl)
+    qsl = wl.query_start_loc
+    out = oracle.attention(wl.q_prefill, kc, vc, wl.block_table_prefill, wl.seq_lens_prefill,
+                           wl.scale, query_start_loc=qsl)
+    for i in range(2):
+        L, C = int(wl.seq_lens_prefill[i]), int(qsl[i + 1] - qsl[i])
+        qi = torch.from_numpy(W.as_f64(wl.q_prefill[qsl[i]:qsl[i + 1]])).transpose(0, 1)
+        K = torch.from_numpy(W.as_f64(wl.contiguous_k_prefill[i])).transpose(0, 1).repeat_interleave(2, 0)
+        V = torch.from_numpy(W.as_f64(wl.contiguous_v_prefill[i])).transpose(0, 1).repeat_interleave(2, 0)
+        mask = torch.arange(L).unsqueeze(0) <= (torch.arange(C).unsqueeze(1) + L - C)
+        ref = torch.nn.functional.scaled_dot_product_attention(qi, K, V, attn_mask=mask, scale=wl.scale)
+        np.testing.assert_allclose(out[qsl[i]:qsl[i + 1]], ref.transpose(0, 1).numpy(), rtol=1e-12, atol=1e-12)
