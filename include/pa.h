@@ -1,8 +1,8 @@
 /*
  * pa.h - C ABI of the GB300 (sm_103a) paged-KV attention library (libpa.so).
  *
- * The KV cache is a pool of fixed-size physical blocks of 16 tokens placed anywhere in
- * device memory; a sequence reaches its blocks through a block table that maps logical
+ * The KV cache is a pool of fixed-size physical blocks of 16 tokens (or 32, 64 or 128
+ * through the *_bs entry points) placed anywhere in device memory; a sequence reaches its blocks through a block table that maps logical
  * block i to a physical block id ("vLLM Internals: From PagedAttention to Removing
  * PagedAttention", section 1.1; "My Understanding of vLLM and PagedAttention", sections
  * "Logical Blocks", "Physical Blocks" and "Block Table"). The table is a dense int32
@@ -12,11 +12,12 @@
  * that "no block" points at, so that padding needs no sentinel ("vLLM: what
  * PagedAttention turned into", section "The block pool").
  *
- * Layouts (all row-major, all device memory, element type given by pa_dtype):
- *   k_cache, v_cache   [num_blocks][num_kv_heads][16][head_dim]  (one (block, head) page
- *                      of 16 x head_dim elements is contiguous)
- *   slot               physical_block * 16 + offset_in_block; position p of a sequence
- *                      lives in logical block p / 16 at offset p % 16 (0-based)
+ * Layouts (all row-major, all device memory, element type given by pa_dtype; BS is the
+ * block size, 16 for the plain entry points and the block_size argument of the *_bs ones):
+ *   k_cache, v_cache   [num_blocks][num_kv_heads][BS][head_dim]  (one (block, head) page
+ *                      of BS x head_dim elements is contiguous)
+ *   slot               physical_block * BS + offset_in_block; position p of a sequence
+ *                      lives in logical block p / BS at offset p % BS (0-based)
  *   q, out (decode)    [num_seqs][num_q_heads][head_dim]
  *   q, out (prefill)   [total_query_tokens][num_q_heads][head_dim], sequences packed in
  *                      the order of query_start_loc
@@ -34,10 +35,10 @@
  *     A failed launch returns PA_ERR_CUDA.
  *   - Device data that the host cannot check (slots, block ids, lengths) is range-checked
  *     by the kernels: an out-of-range slot is not written, an out-of-range block id or a
- *     length beyond max_blocks_per_seq * 16 is not read; each sets a bit in the device
+ *     length beyond max_blocks_per_seq * BS is not read; each sets a bit in the device
  *     error word (pa_get_device_errors). Kernels never trap.
  *   - seq_lens[i] counts every key of sequence i, the current token(s) included.
- *   - Only the first ceil(seq_lens[i] / 16) entries of block-table row i are read; the
+ *   - Only the first ceil(seq_lens[i] / BS) entries of block-table row i are read; the
  *     unused tail of a sequence's last block is never read into a result (its contents
  *     may be anything, NaN included), nor is block 0 unless a table names it.
  */
@@ -74,7 +75,7 @@ typedef enum {
 } pa_dtype;
 
 /* Bits of the device error word. */
-#define PA_DEVERR_SLOT_RANGE   0x1u  /* reshape_and_cache met a slot >= num_blocks * 16   */
+#define PA_DEVERR_SLOT_RANGE   0x1u  /* reshape_and_cache met a slot >= num_blocks * BS   */
 #define PA_DEVERR_BLOCK_RANGE  0x2u  /* a block-table entry outside [0, num_blocks)       */
 #define PA_DEVERR_LEN_RANGE    0x4u  /* a length beyond the table row or max_seq_len      */
 #define PA_DEVERR_WAIT_TIMEOUT 0x8u  /* a bounded pipeline wait gave up (results invalid) */
@@ -99,6 +100,22 @@ PA_API pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_cach
                                const int64_t* slot_mapping, int32_t num_tokens,
                                int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
                                pa_dtype dtype, void* stream);
+
+/*
+ * Block-size variants. The page "vLLM: what PagedAttention turned into" (intro table and
+ * "The problem PagedAttention was actually solving") gives 16 tokens as the block size and
+ * reports sizes from 16 to 128 performing alike. Each *_bs entry point is its plain
+ * counterpart with the block size as an argument: block_size must be 16, 32, 64 or 128
+ * (another positive value returns PA_ERR_UNSUPPORTED, zero or a negative one
+ * PA_ERR_INVALID_ARG), and every "16" of the plain entry point's description (pool layout,
+ * slot arithmetic, table reads, length bound) reads block_size. The kernels walk a block
+ * as block_size / 16 consecutive 16-token pages, so results are bit-identical to the same
+ * keys stored in 16-token blocks. pa_decode_workspace_size does not depend on the block size.
+ */
+PA_API pa_status pa_reshape_and_cache_bs(const void* k, const void* v, void* k_cache, void* v_cache,
+                                         const int64_t* slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
+                                         int32_t head_dim, int32_t num_blocks, int32_t block_size, pa_dtype dtype,
+                                         void* stream);
 
 /*
  * pa_decode_workspace_size: bytes of device scratch that pa_decode needs for this shape on
@@ -143,6 +160,13 @@ PA_API pa_status pa_decode(void* out, const void* q, const void* k_cache, const 
                     int32_t num_blocks, float scale, pa_dtype dtype,
                     void* workspace, size_t workspace_bytes, void* stream);
 
+/* pa_decode with block_size (see the block-size variants above). */
+PA_API pa_status pa_decode_bs(void* out, const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                              int32_t num_seqs, int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                              int32_t head_dim, int32_t num_blocks, int32_t block_size, float scale, pa_dtype dtype,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
 /*
  * pa_prefill_chunk: causal attention for a chunk of new query tokens per sequence, on top
  * of the sequence's earlier context already in the pool (chunked prefill: a long prompt is
@@ -167,6 +191,14 @@ PA_API pa_status pa_prefill_chunk(void* out, const void* q, const void* k_cache,
                            int32_t num_seqs, int32_t max_chunk_len, int32_t max_seq_len,
                            int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                            int32_t num_blocks, float scale, pa_dtype dtype, void* stream);
+
+/* pa_prefill_chunk with block_size (see the block-size variants above). */
+PA_API pa_status pa_prefill_chunk_bs(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                     const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                     const int32_t* query_start_loc, int32_t num_seqs, int32_t max_chunk_len,
+                                     int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                                     int32_t head_dim, int32_t num_blocks, int32_t block_size, float scale,
+                                     pa_dtype dtype, void* stream);
 
 /*
  * pa_decode_noalloc: pa_decode for callers that cannot allocate device memory. The source
@@ -296,6 +328,11 @@ PA_API pa_status pa_sha256(const uint8_t* data, size_t n, uint8_t* out32);
 PA_API pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_pairs, int32_t n_pairs,
                                 int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, pa_dtype dtype,
                                 void* stream);
+
+/* pa_copy_blocks with block_size (see the block-size variants above). */
+PA_API pa_status pa_copy_blocks_bs(void* k_cache, void* v_cache, const int32_t* block_pairs, int32_t n_pairs,
+                                   int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, int32_t block_size,
+                                   pa_dtype dtype, void* stream);
 
 #ifdef __cplusplus
 }

@@ -24,7 +24,10 @@ EXPORTED = ("pa_reshape_and_cache", "pa_decode_workspace_size", "pa_decode", "pa
             "pa_bm_create", "pa_bm_destroy", "pa_bm_num_free_blocks", "pa_bm_add_request", "pa_bm_append_tokens",
             "pa_bm_commit", "pa_bm_fork", "pa_bm_free_request", "pa_bm_get_blocks", "pa_bm_slot_mapping",
             "pa_bm_take_copies", "pa_bm_free_queue", "pa_bm_block_info", "pa_bm_num_blocks_for_memory", "pa_sha256",
-            "pa_copy_blocks")
+            "pa_copy_blocks", "pa_reshape_and_cache_bs", "pa_decode_bs", "pa_prefill_chunk_bs",
+            "pa_copy_blocks_bs")
+#: block sizes the *_bs entry points accept
+BLOCK_SIZES = (16, 32, 64, 128)
 #: size of the library's fixed scratch used by pa_decode_noalloc
 PA_DECODE_NOALLOC_MAX_BYTES = 16 * 1024 * 1024
 
@@ -81,7 +84,14 @@ def load(build_if_needed: bool = True) -> ctypes.CDLL:
                     ("pa_bm_block_info", ctypes.c_int, [vp, i32, pi32, pu8, pi32]),
                     ("pa_bm_num_blocks_for_memory", i64, [sz, ctypes.c_double, i32, i32, i32, ctypes.c_int]),
                     ("pa_sha256", ctypes.c_int, [vp, sz, pu8]),
-                    ("pa_copy_blocks", ctypes.c_int, [vp, vp, vp, i32, i32, i32, i32, ctypes.c_int, vp])):
+                    ("pa_copy_blocks", ctypes.c_int, [vp, vp, vp, i32, i32, i32, i32, ctypes.c_int, vp]),
+                    ("pa_reshape_and_cache_bs", ctypes.c_int, [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                                               ctypes.c_int, vp]),
+                    ("pa_decode_bs", ctypes.c_int, [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32,
+                                                    f32, ctypes.c_int, vp, sz, vp]),
+                    ("pa_prefill_chunk_bs", ctypes.c_int, [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32,
+                                                           i32, i32, i32, f32, ctypes.c_int, vp]),
+                    ("pa_copy_blocks_bs", ctypes.c_int, [vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_int, vp])):
                 fn = getattr(lib, name)
                 fn.restype = res
                 fn.argtypes = args
@@ -127,13 +137,31 @@ def _need_cuda(*ts) -> None:
             raise ValueError("libpa takes contiguous CUDA tensors")
 
 
-def pa_reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, stream=None) -> None:
-    """k, v: [T, H_kv, D]; k_cache, v_cache: [NB, H_kv, 16, D]; slot_mapping: [T] int64."""
+def _use_bs(k_cache, force: bool) -> bool:
+    """The block size is the pool's third dimension; 16 goes through the plain entry point
+    unless the *_bs one is asked for."""
+    return force or int(k_cache.shape[2]) != BLOCK_SIZE
+
+
+def pa_reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, stream=None, _bs: bool = False) -> None:
+    """k, v: [T, H_kv, D]; k_cache, v_cache: [NB, H_kv, BS, D] (BS = block size: 16, 32, 64
+    or 128); slot_mapping: [T] int64."""
     _need_cuda(k, v, k_cache, v_cache, slot_mapping)
     T, H_kv, D = k.shape
-    _check("pa_reshape_and_cache", load().pa_reshape_and_cache(
+    lib = load()
+    if _use_bs(k_cache, _bs):
+        _check("pa_reshape_and_cache_bs", lib.pa_reshape_and_cache_bs(
+            _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), T, H_kv, D, k_cache.shape[0],
+            int(k_cache.shape[2]), _dtype_code(k), _stream(stream)))
+        return
+    _check("pa_reshape_and_cache", lib.pa_reshape_and_cache(
         _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), T, H_kv, D, k_cache.shape[0],
         _dtype_code(k), _stream(stream)))
+
+
+def pa_reshape_and_cache_bs(k, v, k_cache, v_cache, slot_mapping, stream=None) -> None:
+    """pa_reshape_and_cache through the block-size entry point (block size = k_cache.shape[2])."""
+    pa_reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, stream, _bs=True)
 
 
 def pa_decode_workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
@@ -144,26 +172,41 @@ def pa_decode_workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int,
 
 
 def pa_decode(out, q, k_cache, v_cache, block_table, seq_lens, max_seq_len: int, scale: float,
-              workspace=None, stream=None) -> None:
+              workspace=None, stream=None, _bs: bool = False) -> None:
     """out, q: [S, H_q, D]; block_table: [S, max_blocks] int32; seq_lens: [S] int32;
-    workspace: uint8 CUDA tensor of at least pa_decode_workspace_size(...) bytes (or None
-    when that size is 0)."""
+    k_cache, v_cache: [NB, H_kv, BS, D]; workspace: uint8 CUDA tensor of at least
+    pa_decode_workspace_size(...) bytes (or None when that size is 0)."""
     _need_cuda(out, q, k_cache, v_cache, block_table, seq_lens, workspace)
     S, H_q, D = q.shape
     NB, H_kv = k_cache.shape[0], k_cache.shape[1]
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check("pa_decode", load().pa_decode(
+    lib = load()
+    if _use_bs(k_cache, _bs):
+        _check("pa_decode_bs", lib.pa_decode_bs(
+            _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
+            _ptr(seq_lens), S, int(max_seq_len), H_q, H_kv, D, NB, int(k_cache.shape[2]), float(scale),
+            _dtype_code(q), _ptr(workspace), ws_bytes, _stream(stream)))
+        return
+    _check("pa_decode", lib.pa_decode(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
         _ptr(seq_lens), S, int(max_seq_len), H_q, H_kv, D, NB, float(scale), _dtype_code(q), _ptr(workspace),
         ws_bytes, _stream(stream)))
+
+
+def pa_decode_bs(out, q, k_cache, v_cache, block_table, seq_lens, max_seq_len: int, scale: float,
+                 workspace=None, stream=None) -> None:
+    """pa_decode through the block-size entry point (block size = k_cache.shape[2])."""
+    pa_decode(out, q, k_cache, v_cache, block_table, seq_lens, max_seq_len, scale, workspace, stream, _bs=True)
 
 
 def pa_decode_noalloc(out, q, k_cache, v_cache, block_table, seq_lens, max_seq_len: int, scale: float,
                       stream=None) -> None:
     """pa_decode without a workspace argument, for callers that cannot allocate device
     memory: the library's fixed device scratch (PA_DECODE_NOALLOC_MAX_BYTES) is used instead.
-    Calls share that scratch, so they must not overlap on the GPU."""
+    Calls share that scratch, so they must not overlap on the GPU. 16-token blocks only."""
     _need_cuda(out, q, k_cache, v_cache, block_table, seq_lens)
+    if int(k_cache.shape[2]) != BLOCK_SIZE:
+        raise ValueError("pa_decode_noalloc takes 16-token blocks")
     S, H_q, D = q.shape
     NB, H_kv = k_cache.shape[0], k_cache.shape[1]
     _check("pa_decode_noalloc", load().pa_decode_noalloc(
@@ -172,14 +215,21 @@ def pa_decode_noalloc(out, q, k_cache, v_cache, block_table, seq_lens, max_seq_l
 
 
 def pa_prefill_chunk(out, q, k_cache, v_cache, block_table, seq_lens, query_start_loc, max_chunk_len: int,
-                     max_seq_len: int, scale: float, stream=None) -> None:
+                     max_seq_len: int, scale: float, stream=None, _bs: bool = False) -> None:
     """out, q: [T_q, H_q, D]; block_table: [S, max_blocks] int32; seq_lens: [S] int32;
-    query_start_loc: [S + 1] int32."""
+    query_start_loc: [S + 1] int32; k_cache, v_cache: [NB, H_kv, BS, D]."""
     _need_cuda(out, q, k_cache, v_cache, block_table, seq_lens, query_start_loc)
     _, H_q, D = q.shape
     NB, H_kv = k_cache.shape[0], k_cache.shape[1]
     S = seq_lens.shape[0]
-    _check("pa_prefill_chunk", load().pa_prefill_chunk(
+    lib = load()
+    if _use_bs(k_cache, _bs):
+        _check("pa_prefill_chunk_bs", lib.pa_prefill_chunk_bs(
+            _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
+            _ptr(seq_lens), _ptr(query_start_loc), S, int(max_chunk_len), int(max_seq_len), H_q, H_kv, D, NB,
+            int(k_cache.shape[2]), float(scale), _dtype_code(q), _stream(stream)))
+        return
+    _check("pa_prefill_chunk", lib.pa_prefill_chunk(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
         _ptr(seq_lens), _ptr(query_start_loc), S, int(max_chunk_len), int(max_seq_len), H_q, H_kv, D, NB,
         float(scale), _dtype_code(q), _stream(stream)))
@@ -192,13 +242,31 @@ def pa_get_device_errors(clear: bool = True) -> int:
     return int(v.value)
 
 
-def pa_copy_blocks(k_cache, v_cache, block_pairs, stream=None) -> None:
-    """k_cache, v_cache: [NB, H_kv, 16, D]; block_pairs: int32 CUDA tensor [n, 2] of (src, dst)."""
+def pa_prefill_chunk_bs(out, q, k_cache, v_cache, block_table, seq_lens, query_start_loc, max_chunk_len: int,
+                        max_seq_len: int, scale: float, stream=None) -> None:
+    """pa_prefill_chunk through the block-size entry point (block size = k_cache.shape[2])."""
+    pa_prefill_chunk(out, q, k_cache, v_cache, block_table, seq_lens, query_start_loc, max_chunk_len, max_seq_len,
+                     scale, stream, _bs=True)
+
+
+def pa_copy_blocks(k_cache, v_cache, block_pairs, stream=None, _bs: bool = False) -> None:
+    """k_cache, v_cache: [NB, H_kv, BS, D]; block_pairs: int32 CUDA tensor [n, 2] of (src, dst)."""
     _need_cuda(k_cache, v_cache, block_pairs)
-    NB, H_kv, _, D = k_cache.shape
-    _check("pa_copy_blocks", load().pa_copy_blocks(
+    NB, H_kv, BS, D = k_cache.shape
+    lib = load()
+    if _use_bs(k_cache, _bs):
+        _check("pa_copy_blocks_bs", lib.pa_copy_blocks_bs(
+            _ptr(k_cache), _ptr(v_cache), _ptr(block_pairs), block_pairs.shape[0], H_kv, D, NB, int(BS),
+            _dtype_code(k_cache), _stream(stream)))
+        return
+    _check("pa_copy_blocks", lib.pa_copy_blocks(
         _ptr(k_cache), _ptr(v_cache), _ptr(block_pairs), block_pairs.shape[0], H_kv, D, NB, _dtype_code(k_cache),
         _stream(stream)))
+
+
+def pa_copy_blocks_bs(k_cache, v_cache, block_pairs, stream=None) -> None:
+    """pa_copy_blocks through the block-size entry point (block size = k_cache.shape[2])."""
+    pa_copy_blocks(k_cache, v_cache, block_pairs, stream, _bs=True)
 
 
 def pa_sha256(data: bytes) -> bytes:

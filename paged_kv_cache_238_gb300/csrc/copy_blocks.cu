@@ -6,7 +6,7 @@
 //
 // Pure data movement: grid x = pair, grid y = 16-byte chunks of a block; each thread moves
 // one chunk of K and the same chunk of V, coalesced on both sides (a block's K for all heads
-// is H_kv * 16 * head_dim * elem contiguous bytes).
+// is H_kv * block_size * head_dim * elem contiguous bytes).
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(int4* __restrict__ k_c
 
 cudaError_t launch_copy_blocks(const CopyBlocksArgs& a, cudaStream_t stream) {
     if (a.num_pairs == 0) return cudaSuccess;
-    const uint32_t chunks = static_cast<uint32_t>(static_cast<int64_t>(a.num_kv_heads) * kBlock * a.head_dim *
+    const uint32_t chunks = static_cast<uint32_t>(static_cast<int64_t>(a.num_kv_heads) * a.block_size * a.head_dim *
                                                   a.elem_bytes / 16);
     dim3 grid(static_cast<unsigned>(a.num_pairs), (chunks + 255) / 256);
     copy_blocks_kernel<<<grid, 256, 0, stream>>>(static_cast<int4*>(a.k_cache), static_cast<int4*>(a.v_cache),

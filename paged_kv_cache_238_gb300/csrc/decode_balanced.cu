@@ -48,7 +48,7 @@ __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x
 
 // Stage: K page (D/64 swizzled 2 KB boxes), V page, then the segment's query rows.
 __host__ __device__ inline uint32_t bal_stage_bytes(int D, int G) {
-    return align_up(2u * kBlock * D * 2u + static_cast<uint32_t>(G) * D * 2u, 1024u);
+    return align_up(2u * kPageTokens * D * 2u + static_cast<uint32_t>(G) * D * 2u, 1024u);
 }
 
 struct BalLayout {
@@ -255,8 +255,9 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
     __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ block_table,
     int32_t max_blocks, const int32_t* __restrict__ seq_lens, int32_t S, int32_t num_kv_heads, int32_t G,
-    int32_t num_blocks, float scale_log2, int32_t nst, uint32_t stage_bytes, BalWorkspace ws, uint32_t* err) {
-    constexpr uint32_t kPage = kBlock * D * 2;
+    int32_t num_blocks, int32_t sub_log2, float scale_log2, int32_t nst, uint32_t stage_bytes, BalWorkspace ws,
+    uint32_t* err) {
+    constexpr uint32_t kPage = kPageTokens * D * 2;
     constexpr uint32_t kHalves = D / 64;
     constexpr int KS = D / 16;  // k-steps over head_dim
     constexpr int E = D / 32;   // elements per lane in the merges
@@ -276,7 +277,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
     int32_t* lens = reinterpret_cast<int32_t*>(smem + L.lens);
 
     const int32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int32_t cap = max_blocks * kBlock;
+    const int32_t cap = table_tokens(max_blocks, sub_log2);
     const int32_t Hq = G * num_kv_heads;
 
     // Inputs may come from the kernel before this one in the stream (programmatic launch).
@@ -294,7 +295,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
                 len = len < 0 ? 0 : cap;
             }
             lens[s] = len;
-            local += ((len + kBlock - 1) / kBlock) * num_kv_heads;
+            local += ((len + kPageTokens - 1) / kPageTokens) * num_kv_heads;
         }
         int32_t incl = local;
 #pragma unroll
@@ -318,7 +319,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
         int32_t run = base + incl - local;
         for (int32_t s = b; s < e; ++s) {
             prefix[s] = run;
-            run += ((lens[s] + kBlock - 1) / kBlock) * num_kv_heads;
+            run += ((lens[s] + kPageTokens - 1) / kPageTokens) * num_kv_heads;
         }
         if (tid == NTH - 1) prefix[S] = base + incl;
         __syncthreads();
@@ -354,12 +355,12 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
             const int32_t np = (prefix[s + 1] - prefix[s]) / num_kv_heads;
             const int32_t r = u - prefix[s];
             const int32_t h = r / np, j = r - h * np;
-            int32_t phys = __ldg(block_table + static_cast<int64_t>(s) * max_blocks + j);
+            int32_t phys = __ldg(block_table + static_cast<int64_t>(s) * max_blocks + (j >> sub_log2));
             if (phys < 0 || phys >= num_blocks) {
                 raise_error(err, PA_DEVERR_BLOCK_RANGE);
                 phys = 0;
             }
-            return (phys * num_kv_heads + h) * kBlock;
+            return ((((phys * num_kv_heads + h) << sub_log2) + (j & ((1 << sub_log2) - 1))) * kPageTokens);
         };
         int32_t kc = 0;
         int32_t id_cur = lane_row(0);
@@ -455,10 +456,10 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
                 }
                 t_first = t;
             }
-            const int32_t ntok = min(kBlock, wc.len - wc.j * kBlock);
-            if (ntok < kBlock) {
+            const int32_t ntok = min(kPageTokens, wc.len - wc.j * kPageTokens);
+            if (ntok < kPageTokens) {
                 // zero the V rows of the unused tail so that p = 0 contributes exactly nothing
-                const int32_t rows = kBlock - ntok;
+                const int32_t rows = kPageTokens - ntok;
                 for (int32_t c = lane; c < rows * 8 * static_cast<int32_t>(kHalves); c += 32) {
                     const int32_t hf = c / (rows * 8), rem = c - hf * rows * 8;
                     *reinterpret_cast<int4*>(stage + kPage + hf * 2048u + (ntok + rem / 8) * 128u + (rem % 8) * 16u) =
@@ -600,7 +601,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
                 }
             }
             __syncwarp();
-            if (ntok < kBlock) fence_proxy_async_shared();  // generic writes before the next copy
+            if (ntok < kPageTokens) fence_proxy_async_shared();  // generic writes before the next copy
             if (t + nst < n) issue(t + nst);
             wc.advance(prefix, lens, S, num_kv_heads);
         }
@@ -759,18 +760,19 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
 template <int D, int NW, int NH>
 cudaError_t launch_impl(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream) {
     alignas(64) CUtensorMap tm_k, tm_v;
-    const uint64_t rows = static_cast<uint64_t>(a.num_blocks) * a.num_kv_heads * kBlock;
+    // Pool rows of head_dim elements: (block, kv head, token in block).
+    const uint64_t rows = static_cast<uint64_t>(a.num_blocks) * a.num_kv_heads * a.block_size;
     cudaError_t e;
     if (D == 128) {
         // (column within a half, pool row, half): one box is a whole 16-row page, stored as
         // two 16 x 128-byte swizzled halves
-        e = encode_bf16_3d_sw128(&tm_k, a.k_cache, 64, rows, 2, D * 2, 128, 64, kBlock, 2);
+        e = encode_bf16_3d_sw128(&tm_k, a.k_cache, 64, rows, 2, D * 2, 128, 64, kPageTokens, 2);
         if (e != cudaSuccess) return e;
-        e = encode_bf16_3d_sw128(&tm_v, a.v_cache, 64, rows, 2, D * 2, 128, 64, kBlock, 2);
+        e = encode_bf16_3d_sw128(&tm_v, a.v_cache, 64, rows, 2, D * 2, 128, 64, kPageTokens, 2);
     } else {
-        e = encode_bf16_2d_sw128(&tm_k, a.k_cache, D, rows, 64, kBlock);
+        e = encode_bf16_2d_sw128(&tm_k, a.k_cache, D, rows, 64, kPageTokens);
         if (e != cudaSuccess) return e;
-        e = encode_bf16_2d_sw128(&tm_v, a.v_cache, D, rows, 64, kBlock);
+        e = encode_bf16_2d_sw128(&tm_v, a.v_cache, D, rows, 64, kPageTokens);
     }
     if (e != cudaSuccess) return e;
     const int32_t G = a.num_q_heads / a.num_kv_heads;
@@ -793,8 +795,9 @@ cudaError_t launch_impl(const DecodeArgs& a, const DecodePlan& plan, cudaStream_
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, decode_balanced_kernel<D, NW, NH>, tm_k, tm_v, static_cast<__nv_bfloat16*>(a.out),
                               static_cast<const __nv_bfloat16*>(a.q), a.block_table, a.max_blocks_per_seq,
-                              a.seq_lens, a.num_seqs, a.num_kv_heads, G, a.num_blocks, a.scale * kLog2e, plan.stages,
-                              plan.stage_bytes, ws, a.err);
+                              a.seq_lens, a.num_seqs, a.num_kv_heads, G, a.num_blocks,
+                              block_size_log2(a.block_size) - 4, a.scale * kLog2e, plan.stages, plan.stage_bytes, ws,
+                              a.err);
 }
 
 template <int D, int NW>

@@ -58,8 +58,9 @@ __global__ void __launch_bounds__(kSimtThreads) decode_simt_kernel(
     const int32_t* __restrict__ block_table, int32_t max_blocks, const int32_t* __restrict__ seq_lens,
     int32_t num_q_heads, int32_t num_kv_heads, int32_t num_blocks, float scale_log2, int32_t part_tokens,
     int32_t num_parts, int32_t head_chunks, float* __restrict__ ws_o, float* __restrict__ ws_ml,
-    const int32_t* __restrict__ query_start_loc, int32_t num_seqs, uint32_t* err) {
+    const int32_t* __restrict__ query_start_loc, int32_t num_seqs, int32_t sub_log2, uint32_t* err) {
     constexpr int E = D / 32;  // elements per lane
+    const int32_t cap_tokens = table_tokens(max_blocks, sub_log2);
     const int32_t row = blockIdx.x;  // query row: a sequence (decode) or a chunk token (prefill)
     const int32_t hk = blockIdx.y / head_chunks;
     const int32_t g0 = (blockIdx.y % head_chunks) * kSimtHeads;
@@ -70,7 +71,7 @@ __global__ void __launch_bounds__(kSimtThreads) decode_simt_kernel(
 
     int32_t s = row, len;
     if (query_start_loc == nullptr) {
-        len = clamped_len(seq_lens, s, min(max_blocks * kBlock, num_parts * part_tokens), err);
+        len = clamped_len(seq_lens, s, min(cap_tokens, num_parts * part_tokens), err);
     } else {
         // prefill: chunk row r of sequence s sits at position seq_len - C + r and sees keys
         // 0..position, i.e. a query of visible length seq_len - C + r + 1
@@ -82,7 +83,7 @@ __global__ void __launch_bounds__(kSimtThreads) decode_simt_kernel(
         }
         s = lo;
         const int32_t q0 = __ldg(query_start_loc + s), chunk = __ldg(query_start_loc + s + 1) - q0;
-        const int32_t total = clamped_len(seq_lens, s, min(max_blocks * kBlock, num_parts * part_tokens), err);
+        const int32_t total = clamped_len(seq_lens, s, min(cap_tokens, num_parts * part_tokens), err);
         len = total - chunk + (row - q0) + 1;
         if (len < 1 || chunk > total) {
             raise_error(err, PA_DEVERR_LEN_RANGE);
@@ -121,14 +122,16 @@ __global__ void __launch_bounds__(kSimtThreads) decode_simt_kernel(
         for (int e = 0; e < E; ++e) acc[g][e] = 0.f;
     }
 
-    for (int32_t page = t0 / kBlock + warp; page * kBlock < t1; page += kSimtThreads / 32) {
-        const int32_t phys = __ldg(block_table + static_cast<int64_t>(s) * max_blocks + page);
+    for (int32_t page = t0 / kPageTokens + warp; page * kPageTokens < t1; page += kSimtThreads / 32) {
+        const int32_t phys = __ldg(block_table + static_cast<int64_t>(s) * max_blocks + (page >> sub_log2));
         if (phys < 0 || phys >= num_blocks) {
             raise_error(err, PA_DEVERR_BLOCK_RANGE);
             continue;
         }
-        const int32_t ntok = min(kBlock, t1 - page * kBlock);
-        const int64_t base = ((static_cast<int64_t>(phys) * num_kv_heads + hk) * kBlock) * D + lane * E;
+        const int32_t ntok = min(kPageTokens, t1 - page * kPageTokens);
+        const int64_t base =
+            ((((static_cast<int64_t>(phys) * num_kv_heads + hk) << sub_log2) + (page & ((1 << sub_log2) - 1))) *
+             kPageTokens) * D + lane * E;
         for (int32_t j = 0; j < ntok; ++j) {
             float kr[E], vr[E];
 #pragma unroll
@@ -238,10 +241,11 @@ static cudaError_t launch_simt_impl(const DecodeArgs& a, const DecodePlan& plan,
         static_cast<T*>(a.out), static_cast<const T*>(a.q), static_cast<const T*>(a.k_cache),
         static_cast<const T*>(a.v_cache), a.block_table, a.max_blocks_per_seq, a.seq_lens, a.num_q_heads,
         a.num_kv_heads, a.num_blocks, scale_log2, plan.partition_tokens, plan.num_partitions, plan.head_chunks,
-        ws_o, ws_ml, nullptr, a.num_seqs, a.err);
+        ws_o, ws_ml, nullptr, a.num_seqs, block_size_log2(a.block_size) - 4, a.err);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || plan.num_partitions == 1) return e;
-    const int32_t cap = min(a.max_blocks_per_seq * kBlock, plan.num_partitions * plan.partition_tokens);
+    const int32_t cap = min(table_tokens(a.max_blocks_per_seq, block_size_log2(a.block_size) - 4),
+                            plan.num_partitions * plan.partition_tokens);
     decode_simt_reduce_kernel<T, D><<<dim3(a.num_seqs, a.num_q_heads), D, 0, stream>>>(
         static_cast<T*>(a.out), a.seq_lens, cap, a.num_q_heads, plan.partition_tokens, plan.num_partitions, ws_o,
         ws_ml);
@@ -253,13 +257,13 @@ static cudaError_t launch_simt_prefill(const PrefillArgs& a, int32_t total_rows,
     // One CTA per (chunk row, kv head x head chunk), whole visible length: no workspace.
     const int32_t G = a.num_q_heads / a.num_kv_heads;
     const int32_t head_chunks = (G + kSimtHeads - 1) / kSimtHeads;
-    const int32_t pt = max(kBlock, ((a.max_seq_len + kBlock - 1) / kBlock) * kBlock);
+    const int32_t pt = max(kPageTokens, ((a.max_seq_len + kPageTokens - 1) / kPageTokens) * kPageTokens);
     dim3 grid(total_rows, a.num_kv_heads * head_chunks, 1);
     decode_simt_kernel<T, D><<<grid, kSimtThreads, 0, stream>>>(
         static_cast<T*>(a.out), static_cast<const T*>(a.q), static_cast<const T*>(a.k_cache),
         static_cast<const T*>(a.v_cache), a.block_table, a.max_blocks_per_seq, a.seq_lens, a.num_q_heads,
         a.num_kv_heads, a.num_blocks, a.scale * kLog2e, pt, 1, head_chunks, nullptr, nullptr, a.query_start_loc,
-        a.num_seqs, a.err);
+        a.num_seqs, block_size_log2(a.block_size) - 4, a.err);
     return cudaGetLastError();
 }
 

@@ -65,17 +65,18 @@ bool dtype_ok(pa_dtype dt) { return dt == PA_F32 || dt == PA_BF16; }
 // Shared checks of the attention entry points.
 pa_status check_attention_shape(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                  int32_t num_blocks, int32_t max_blocks_per_seq, int32_t max_seq_len,
-                                 pa_dtype dtype) {
+                                 pa_dtype dtype, int32_t block_size) {
+    if (!block_size_ok(block_size)) return block_size > 0 ? PA_ERR_UNSUPPORTED : PA_ERR_INVALID_ARG;
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 || max_blocks_per_seq <= 0 ||
         max_seq_len < 0)
         return PA_ERR_INVALID_ARG;
     if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
     if (!dtype_ok(dtype)) return PA_ERR_INVALID_ARG;
     if (head_dim != 64 && head_dim != 128) return head_dim > 0 ? PA_ERR_UNSUPPORTED : PA_ERR_INVALID_ARG;
-    if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_blocks_per_seq) * PA_BLOCK_SIZE)
+    if (static_cast<int64_t>(max_seq_len) > static_cast<int64_t>(max_blocks_per_seq) * block_size)
         return PA_ERR_INVALID_ARG;
     // Pool rows (block, head, token) are addressed with 32-bit coordinates.
-    if (static_cast<int64_t>(num_blocks) * num_kv_heads * PA_BLOCK_SIZE > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(num_blocks) * num_kv_heads * block_size > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
     return PA_OK;
 }
 
@@ -147,10 +148,12 @@ PA_API const char* pa_status_string(pa_status status) {
     return "PA_UNKNOWN_STATUS";
 }
 
-PA_API pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
-                                      const int64_t* slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
-                                      int32_t head_dim, int32_t num_blocks, pa_dtype dtype, void* stream) {
+PA_API pa_status pa_reshape_and_cache_bs(const void* k, const void* v, void* k_cache, void* v_cache,
+                                         const int64_t* slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
+                                         int32_t head_dim, int32_t num_blocks, int32_t block_size, pa_dtype dtype,
+                                         void* stream) {
     if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0) return PA_ERR_INVALID_ARG;
+    if (!block_size_ok(block_size)) return block_size > 0 ? PA_ERR_UNSUPPORTED : PA_ERR_INVALID_ARG;
     if (!dtype_ok(dtype)) return PA_ERR_INVALID_ARG;
     if ((head_dim * elem_bytes(dtype)) % 16 != 0) return PA_ERR_UNSUPPORTED;
     if (num_tokens == 0) return PA_OK;
@@ -163,16 +166,24 @@ PA_API pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_cach
     DeviceCache* dev = nullptr;
     if (device_cache(&dev) != cudaSuccess) return PA_ERR_CUDA;
     ReshapeArgs a{k, v, k_cache, v_cache, slot_mapping, num_tokens, num_kv_heads, head_dim, num_blocks,
-                  elem_bytes(dtype), dev->err};
+                  elem_bytes(dtype), block_size, dev->err};
     return launch_reshape_and_cache(a, dev->info.num_sms, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? PA_OK
                : PA_ERR_CUDA;
 }
 
-PA_API pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_pairs, int32_t n_pairs,
-                                int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, pa_dtype dtype,
-                                void* stream) {
+PA_API pa_status pa_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
+                                      const int64_t* slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
+                                      int32_t head_dim, int32_t num_blocks, pa_dtype dtype, void* stream) {
+    return pa_reshape_and_cache_bs(k, v, k_cache, v_cache, slot_mapping, num_tokens, num_kv_heads, head_dim,
+                                   num_blocks, PA_BLOCK_SIZE, dtype, stream);
+}
+
+PA_API pa_status pa_copy_blocks_bs(void* k_cache, void* v_cache, const int32_t* block_pairs, int32_t n_pairs,
+                                   int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, int32_t block_size,
+                                   pa_dtype dtype, void* stream) {
     if (n_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0) return PA_ERR_INVALID_ARG;
+    if (!block_size_ok(block_size)) return block_size > 0 ? PA_ERR_UNSUPPORTED : PA_ERR_INVALID_ARG;
     if (!dtype_ok(dtype)) return PA_ERR_INVALID_ARG;
     if ((head_dim * elem_bytes(dtype)) % 16 != 0) return PA_ERR_UNSUPPORTED;
     if (n_pairs == 0) return PA_OK;
@@ -180,19 +191,26 @@ PA_API pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* blo
     if (!k_cache || !v_cache || !block_pairs) return PA_ERR_INVALID_ARG;
     if (!aligned16(k_cache) || !aligned16(v_cache) || (reinterpret_cast<uintptr_t>(block_pairs) & 3u))
         return PA_ERR_INVALID_ARG;
-    const int64_t chunks = static_cast<int64_t>(num_kv_heads) * 16 * head_dim * elem_bytes(dtype) / 16;
+    const int64_t chunks = static_cast<int64_t>(num_kv_heads) * block_size * head_dim * elem_bytes(dtype) / 16;
     if (chunks > 0x7fffffffLL || (chunks + 255) / 256 > 65535) return PA_ERR_UNSUPPORTED;
     DeviceCache* dev = nullptr;
     if (device_cache(&dev) != cudaSuccess) return PA_ERR_CUDA;
     CopyBlocksArgs a{k_cache, v_cache, block_pairs, n_pairs, num_kv_heads, head_dim, num_blocks, elem_bytes(dtype),
-                     dev->err};
+                     block_size, dev->err};
     return launch_copy_blocks(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+PA_API pa_status pa_copy_blocks(void* k_cache, void* v_cache, const int32_t* block_pairs, int32_t n_pairs,
+                                int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, pa_dtype dtype,
+                                void* stream) {
+    return pa_copy_blocks_bs(k_cache, v_cache, block_pairs, n_pairs, num_kv_heads, head_dim, num_blocks,
+                             PA_BLOCK_SIZE, dtype, stream);
 }
 
 PA_API size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                        int32_t head_dim, int32_t max_seq_len, pa_dtype dtype) {
     if (check_attention_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, 1, (max_seq_len + 15) / 16 + 1,
-                              max_seq_len, dtype) != PA_OK)
+                              max_seq_len, dtype, PA_BLOCK_SIZE) != PA_OK)
         return 0;
     DeviceCache* dev = nullptr;
     if (device_cache(&dev) != cudaSuccess) return 0;
@@ -200,13 +218,13 @@ PA_API size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, in
         .workspace_bytes;
 }
 
-PA_API pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
-                           const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
-                           int32_t num_seqs, int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
-                           int32_t head_dim, int32_t num_blocks, float scale, pa_dtype dtype, void* workspace,
-                           size_t workspace_bytes, void* stream) {
+PA_API pa_status pa_decode_bs(void* out, const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                              int32_t num_seqs, int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                              int32_t head_dim, int32_t num_blocks, int32_t block_size, float scale, pa_dtype dtype,
+                              void* workspace, size_t workspace_bytes, void* stream) {
     pa_status st = check_attention_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks,
-                                         max_blocks_per_seq, max_seq_len, dtype);
+                                         max_blocks_per_seq, max_seq_len, dtype, block_size);
     if (st != PA_OK) return st;
     if (num_seqs == 0) return PA_OK;
     if (!out || !q || !k_cache || !v_cache || !block_table || !seq_lens) return PA_ERR_INVALID_ARG;
@@ -220,18 +238,28 @@ PA_API pa_status pa_decode(void* out, const void* q, const void* k_cache, const 
         return PA_ERR_INVALID_ARG;
     DecodeArgs a{out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
                  num_q_heads, num_kv_heads, head_dim, num_blocks, scale, dtype, workspace, workspace_bytes,
-                 dev->err};
+                 dev->err, block_size};
     return launch_decode(a, plan, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
-PA_API pa_status pa_prefill_chunk(void* out, const void* q, const void* k_cache, const void* v_cache,
-                                  const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
-                                  const int32_t* query_start_loc, int32_t num_seqs, int32_t max_chunk_len,
-                                  int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
-                                  int32_t head_dim, int32_t num_blocks, float scale, pa_dtype dtype,
-                                  void* stream) {
+PA_API pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                           int32_t num_seqs, int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                           int32_t head_dim, int32_t num_blocks, float scale, pa_dtype dtype, void* workspace,
+                           size_t workspace_bytes, void* stream) {
+    return pa_decode_bs(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
+                        num_q_heads, num_kv_heads, head_dim, num_blocks, PA_BLOCK_SIZE, scale, dtype, workspace,
+                        workspace_bytes, stream);
+}
+
+PA_API pa_status pa_prefill_chunk_bs(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                     const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                     const int32_t* query_start_loc, int32_t num_seqs, int32_t max_chunk_len,
+                                     int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                                     int32_t head_dim, int32_t num_blocks, int32_t block_size, float scale,
+                                     pa_dtype dtype, void* stream) {
     pa_status st = check_attention_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks,
-                                         max_blocks_per_seq, max_seq_len, dtype);
+                                         max_blocks_per_seq, max_seq_len, dtype, block_size);
     if (st != PA_OK) return st;
     if (max_chunk_len < 0 || max_chunk_len > max_seq_len) return PA_ERR_INVALID_ARG;
     if (num_seqs == 0 || max_chunk_len == 0) return PA_OK;
@@ -246,8 +274,19 @@ PA_API pa_status pa_prefill_chunk(void* out, const void* q, const void* k_cache,
     if (device_cache(&dev) != cudaSuccess) return PA_ERR_CUDA;
     PrefillArgs a{out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens, query_start_loc, num_seqs,
                   max_chunk_len, max_seq_len, num_q_heads, num_kv_heads, head_dim, num_blocks, scale, dtype,
-                  dev->err};
+                  dev->err, block_size};
     return launch_prefill(a, dev->info, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+PA_API pa_status pa_prefill_chunk(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                  const int32_t* query_start_loc, int32_t num_seqs, int32_t max_chunk_len,
+                                  int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t num_blocks, float scale, pa_dtype dtype,
+                                  void* stream) {
+    return pa_prefill_chunk_bs(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens, query_start_loc,
+                               num_seqs, max_chunk_len, max_seq_len, num_q_heads, num_kv_heads, head_dim, num_blocks,
+                               PA_BLOCK_SIZE, scale, dtype, stream);
 }
 
 PA_API pa_status pa_get_device_errors(uint32_t* errors, int32_t clear) {

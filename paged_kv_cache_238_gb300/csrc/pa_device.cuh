@@ -11,7 +11,16 @@
 
 namespace pa {
 
-constexpr int kBlock = 16;  // tokens per physical block
+// Tokens per page: the unit every attention kernel walks. A physical block of block_size
+// tokens (16, 32, 64 or 128) is block_size / 16 consecutive pages of one (block, kv head).
+constexpr int kPageTokens = 16;
+
+// Tokens a block-table row of max_blocks entries addresses (sub_log2 = log2(block_size / 16)),
+// saturated to the int32 range.
+__host__ __device__ __forceinline__ int32_t table_tokens(int32_t max_blocks, int32_t sub_log2) {
+    const int64_t t = static_cast<int64_t>(max_blocks) << (4 + sub_log2);
+    return t > 0x7fffffffLL ? 0x7fffffff : static_cast<int32_t>(t);
+}
 
 // ------------------------------------------------------------------------------------------
 // error word

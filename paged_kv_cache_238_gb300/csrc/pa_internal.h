@@ -10,6 +10,12 @@
 
 namespace pa {
 
+// Block sizes the kernels accept: powers of two from 16 to 128 tokens. The kernels walk a
+// block as block_size / 16 pages of 16 tokens; page j of a sequence is sub-page
+// j % (block_size / 16) of logical block j / (block_size / 16).
+inline bool block_size_ok(int32_t bs) { return bs == 16 || bs == 32 || bs == 64 || bs == 128; }
+inline int block_size_log2(int32_t bs) { return bs == 128 ? 7 : bs == 64 ? 6 : bs == 32 ? 5 : 4; }
+
 // ------------------------------------------------------------------------------------------
 // reshape_and_cache
 // ------------------------------------------------------------------------------------------
@@ -21,6 +27,7 @@ struct ReshapeArgs {
     const int64_t* slot_mapping;
     int32_t num_tokens, num_kv_heads, head_dim, num_blocks;
     int32_t elem_bytes;
+    int32_t block_size;  // tokens per block: 16, 32, 64 or 128
     uint32_t* err;
 };
 cudaError_t launch_reshape_and_cache(const ReshapeArgs& a, int num_sms, cudaStream_t stream);
@@ -33,6 +40,7 @@ struct CopyBlocksArgs {
     void* v_cache;
     const int32_t* pairs;  // device [num_pairs][2] (src, dst)
     int32_t num_pairs, num_kv_heads, head_dim, num_blocks, elem_bytes;
+    int32_t block_size;
     uint32_t* err;
 };
 cudaError_t launch_copy_blocks(const CopyBlocksArgs& a, cudaStream_t stream);
@@ -54,6 +62,7 @@ struct DecodeArgs {
     void* workspace;
     size_t workspace_bytes;
     uint32_t* err;
+    int32_t block_size;  // tokens per block: 16, 32, 64 or 128
 };
 
 enum DecodePath : int {
@@ -113,6 +122,7 @@ struct PrefillArgs {
     float scale;
     pa_dtype dtype;
     uint32_t* err;
+    int32_t block_size;  // tokens per block: 16, 32, 64 or 128
 };
 // total_rows: number of chunk rows (query_start_loc[num_seqs]); the host cannot read it, so
 // the caller passes an upper bound (grid rows past the end exit at once).

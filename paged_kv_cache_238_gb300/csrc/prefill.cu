@@ -105,7 +105,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
     __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ block_table,
     int32_t max_blocks, const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ query_start_loc,
-    int32_t num_kv_heads, int32_t num_blocks, float scale_log2, uint32_t* err) {
+    int32_t num_kv_heads, int32_t num_blocks, int32_t sub_log2, float scale_log2, uint32_t* err) {
     constexpr int TT = kTcRows / G;  // chunk tokens per Q tile
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
     const int32_t L = __ldg(seq_lens + seq);
     const int32_t t0a = 2 * pair * TT, t0b = t0a + TT;
     if (t0a >= C) return;  // uniform over the CTA
-    if (C > L || L > max_blocks * kBlock || C < 0) {
+    if (C > L || L > table_tokens(max_blocks, sub_log2) || C < 0) {
         if (tid == 0) raise_error(err, PA_DEVERR_LEN_RANGE);
         return;
     }
@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
     const int32_t n_kv_a = (P0 + min(t0a + TT, C) - 1) / kTcKeys + 1;
     const int32_t n_kv_b = active_b ? (P0 + min(t0b + TT, C) - 1) / kTcKeys + 1 : 0;
     const int32_t n_kv = max(n_kv_a, n_kv_b);
-    const int32_t npages = (L + kBlock - 1) / kBlock;
+    const int32_t npages = (L + kPageTokens - 1) / kPageTokens;
 
     if (tid == 0) {
         *abort_flag = 0;
@@ -210,13 +210,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
         auto page_row = [&](int32_t pg) -> int32_t {
             int32_t phys = 0;  // keys past the sequence end read the null block; masked later
             if (pg < npages) {
-                phys = __ldg(block_table + static_cast<int64_t>(seq) * max_blocks + pg);
+                phys = __ldg(block_table + static_cast<int64_t>(seq) * max_blocks + (pg >> sub_log2));
                 if (phys < 0 || phys >= num_blocks) {
                     raise_error(err, PA_DEVERR_BLOCK_RANGE);
                     phys = 0;
                 }
             }
-            return (phys * num_kv_heads + h) * kBlock;
+            return (((phys * num_kv_heads + h) << sub_log2) + (pg & ((1 << sub_log2) - 1))) * kPageTokens;
         };
         int32_t win = 0;
         int32_t row_cur = page_row(lane), row_nxt = page_row(32 + lane);
@@ -485,10 +485,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
 template <int G>
 cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t stream) {
     alignas(64) CUtensorMap tm_k, tm_v;
-    const uint64_t rows = static_cast<uint64_t>(a.num_blocks) * a.num_kv_heads * kBlock;
-    cudaError_t e = encode_bf16_2d_sw128(&tm_k, a.k_cache, kTcD, rows, 64, kBlock);
+    const uint64_t rows = static_cast<uint64_t>(a.num_blocks) * a.num_kv_heads * a.block_size;
+    cudaError_t e = encode_bf16_2d_sw128(&tm_k, a.k_cache, kTcD, rows, 64, kPageTokens);
     if (e != cudaSuccess) return e;
-    e = encode_bf16_2d_sw128(&tm_v, a.v_cache, kTcD, rows, 64, kBlock);
+    e = encode_bf16_2d_sw128(&tm_v, a.v_cache, kTcD, rows, 64, kPageTokens);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(prefill_tc_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(TcSmem::total));
@@ -499,7 +499,8 @@ cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t stream) {
     dim3 grid(pairs, a.num_kv_heads, a.num_seqs);
     prefill_tc_kernel<G><<<grid, kTcThreads, TcSmem::total, stream>>>(
         tm_k, tm_v, static_cast<__nv_bfloat16*>(a.out), static_cast<const __nv_bfloat16*>(a.q), a.block_table,
-        a.max_blocks_per_seq, a.seq_lens, a.query_start_loc, a.num_kv_heads, a.num_blocks, a.scale * kLog2e, a.err);
+        a.max_blocks_per_seq, a.seq_lens, a.query_start_loc, a.num_kv_heads, a.num_blocks,
+        block_size_log2(a.block_size) - 4, a.scale * kLog2e, a.err);
     return cudaGetLastError();
 }
 

@@ -2,8 +2,9 @@
 //
 // New K and V entries are added to the cache as tokens are produced ("My Understanding of
 // vLLM and PagedAttention", "Step 3 - Tokens Generated Sequentially"); the destination of
-// token t is the int64 slot slot_mapping[t] = physical_block * 16 + offset ("vLLM: what
-// PagedAttention turned into", "The problem PagedAttention was actually solving").
+// token t is the int64 slot slot_mapping[t] = physical_block * block_size + offset ("vLLM:
+// what PagedAttention turned into", "The problem PagedAttention was actually solving"; the
+// block size is 16 by default, and the same page reports 16 to 128 working alike).
 //
 // Pure data movement: each thread moves one 16-byte chunk of a (token, kv head) row of K and
 // the same chunk of V. Loads of the new rows are streaming (read once); stores keep the
@@ -23,7 +24,7 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const int4* __re
                                                                 const int64_t* __restrict__ slot_mapping,
                                                                 uint32_t num_items, uint32_t chunks_per_row,
                                                                 uint32_t num_kv_heads, int64_t num_slots,
-                                                                uint32_t* err) {
+                                                                uint32_t bs_log2, uint32_t* err) {
     // Programmatic launch: wait for the kernel before this one (it may still read the pool or
     // produce k, v and the slots), then let the next kernel's grid be scheduled.
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -40,9 +41,9 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const int4* __re
             raise_error(err, PA_DEVERR_SLOT_RANGE);
             continue;
         }
-        const int64_t block = slot / kBlock;
-        const int64_t offset = slot - block * kBlock;
-        const int64_t dst = ((block * num_kv_heads + h) * kBlock + offset) * chunks_per_row + c;
+        const int64_t block = slot >> bs_log2;
+        const int64_t offset = slot - (block << bs_log2);
+        const int64_t dst = (((block * num_kv_heads + h) << bs_log2) + offset) * chunks_per_row + c;
         const int4 kv = __ldcs(k + i);
         const int4 vv = __ldcs(v + i);
         k_cache[dst] = kv;
@@ -76,7 +77,8 @@ cudaError_t launch_reshape_and_cache(const ReshapeArgs& a, int num_sms, cudaStre
                               static_cast<const int4*>(a.v), static_cast<int4*>(a.k_cache),
                               static_cast<int4*>(a.v_cache), a.slot_mapping, static_cast<uint32_t>(num_items),
                               static_cast<uint32_t>(chunks_per_row), static_cast<uint32_t>(a.num_kv_heads),
-                              static_cast<int64_t>(a.num_blocks) * kBlock, a.err);
+                              static_cast<int64_t>(a.num_blocks) * a.block_size,
+                              static_cast<uint32_t>(block_size_log2(a.block_size)), a.err);
 }
 
 }  // namespace pa

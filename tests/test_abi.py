@@ -132,3 +132,35 @@ def test_library_does_not_link_the_oracle():
         with pytest.raises(AttributeError):
             getattr(lib, sym)
     assert isinstance(lib, ctypes.CDLL)
+
+
+def _decode_bs(lib, bs, **kw):
+    args = dict(out=FAKE, q=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, mb=4, lens=FAKE, S=2, max_len=64, Hq=8, Hkv=2,
+                D=128, NB=16, scale=0.1, dt=B.PA_BF16, ws=FAKE, ws_bytes=1 << 20, stream=None)
+    args.update(kw)
+    return lib.pa_decode_bs(args["out"], args["q"], args["kc"], args["vc"], args["bt"], args["mb"], args["lens"],
+                            args["S"], args["max_len"], args["Hq"], args["Hkv"], args["D"], args["NB"], bs,
+                            args["scale"], args["dt"], args["ws"], args["ws_bytes"], args["stream"])
+
+
+@pytest.mark.parametrize("bs,kw,expect", [
+    (48, {}, B.PA_ERR_UNSUPPORTED),                      # not a power of two in 16..128
+    (256, {}, B.PA_ERR_UNSUPPORTED),
+    (8, {}, B.PA_ERR_UNSUPPORTED),
+    (0, {}, B.PA_ERR_INVALID_ARG),
+    (-16, {}, B.PA_ERR_INVALID_ARG),
+    (32, dict(max_len=129), B.PA_ERR_INVALID_ARG),        # beyond max_blocks * 32
+    (128, dict(NB=1 << 23, Hkv=2), B.PA_ERR_UNSUPPORTED),  # pool rows beyond 32-bit coordinates
+    (64, dict(S=0, out=None, q=None), B.PA_OK),
+])
+def test_decode_bs_checks_the_block_size(bs, kw, expect):
+    assert _decode_bs(B.load(), bs, **kw) == expect
+
+
+@pytest.mark.parametrize("bs,expect", [(48, B.PA_ERR_UNSUPPORTED), (0, B.PA_ERR_INVALID_ARG)])
+def test_other_bs_entry_points_check_the_block_size(bs, expect):
+    lib = B.load()
+    assert lib.pa_reshape_and_cache_bs(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 128, 8, bs, B.PA_BF16, None) == expect
+    assert lib.pa_copy_blocks_bs(FAKE, FAKE, FAKE, 2, 2, 128, 8, bs, B.PA_BF16, None) == expect
+    assert lib.pa_prefill_chunk_bs(FAKE, FAKE, FAKE, FAKE, FAKE, 4, FAKE, FAKE, 2, 16, 64, 8, 2, 128, 16, bs, 0.1,
+                                   B.PA_BF16, None) == expect
