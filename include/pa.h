@@ -229,6 +229,76 @@ PA_API pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache
                                    int32_t num_blocks, float scale, pa_dtype dtype, void* stream);
 
 /*
+ * pa_step: one whole mixed step of the serving loop in one call: write the step's new K/V
+ * into the pool, then chunked-prefill attention for the prefill sequences and decode
+ * attention for the decode sequences, with the two attention kernels running side by side.
+ * The pages make the per-step work a fixed launch sequence with no host round trip ("vLLM:
+ * what PagedAttention turned into", "The scheduler" and the model-runner rewrite: persistent
+ * buffers and captured graphs remove per-step CPU work); a step mixes prefill chunks with
+ * decode tokens ("vLLM Internals", section 2, chunked prefill).
+ *
+ * Results are those of the three separate calls (pa_reshape_and_cache_bs, then
+ * pa_prefill_chunk_bs and pa_decode_bs on the same pool). Decode is bound by HBM and
+ * prefill by the tensor cores, so when both are present and decode takes the bf16
+ * persistent path, the decode kernel is given decode_sms SMs and prefill runs on the others
+ * at the same time:
+ *   stream:  reshape_and_cache -> decode (decode_sms persistent CTAs) -> [join]
+ *   side:                     +-> prefill ---------------------------+
+ * The side stream and two fork/join events are the library's own, one set per device,
+ * created by the first call on that device (make it before any stream capture); the
+ * fork/join goes through them under a lock, so pa_step is capturable into a CUDA graph
+ * (the side stream joins the capture) and calls from several threads serialise their
+ * prefills on the one side stream. Otherwise (no prefill, no decode, or a decode shape that
+ * takes the general path) the kernels run one after another on `stream`.
+ *
+ * A part with zero sequences (or zero new tokens) is skipped and its pointers may be NULL.
+ * Every argument is checked as the separate entry point would check it before anything is
+ * launched. decode_sms: 0 = half of the device's SMs; otherwise 1..num_SMs (larger values are
+ * clamped). workspace: >= pa_decode_workspace_size(num_decode_seqs, ...) bytes, as for
+ * pa_decode. timing_events: NULL, or six cudaEvent_t (each may be NULL) recorded before and
+ * after reshape_and_cache, prefill and decode on the stream each kernel runs on, for the
+ * caller's profiling; they are recorded as external events, so under stream capture they
+ * become event-record nodes of the graph (an event between two kernels stops the later one
+ * from launching early).
+ */
+typedef struct {
+    /* the pool and the attention shape shared by every part */
+    void* k_cache;
+    void* v_cache;
+    int32_t num_blocks, block_size;            /* block_size: 16, 32, 64 or 128           */
+    int32_t num_q_heads, num_kv_heads, head_dim;
+    float scale;
+    pa_dtype dtype;
+    /* new tokens of the step (pa_reshape_and_cache) */
+    const void* k_new;
+    const void* v_new;
+    const int64_t* slot_mapping;
+    int32_t num_new_tokens;
+    /* chunked-prefill part (pa_prefill_chunk) */
+    void* prefill_out;
+    const void* prefill_q;
+    const int32_t* prefill_block_table;
+    int32_t prefill_max_blocks_per_seq;
+    const int32_t* prefill_seq_lens;
+    const int32_t* query_start_loc;
+    int32_t num_prefill_seqs, max_chunk_len, prefill_max_seq_len;
+    /* decode part (pa_decode) */
+    void* decode_out;
+    const void* decode_q;
+    const int32_t* decode_block_table;
+    int32_t decode_max_blocks_per_seq;
+    const int32_t* decode_seq_lens;
+    int32_t num_decode_seqs, decode_max_seq_len;
+    void* workspace;
+    size_t workspace_bytes;
+    /* scheduling */
+    int32_t decode_sms;
+    void* const* timing_events;
+} pa_step_desc;
+
+PA_API pa_status pa_step(const pa_step_desc* step, void* stream);
+
+/*
  * pa_get_device_errors: read the device error word of the current device (PA_DEVERR_*
  * bits OR-ed by the kernels since the last clear) into *errors, and clear it when
  * `clear` is non-zero. Synchronises the current device. The library owns the word.

@@ -25,7 +25,7 @@ EXPORTED = ("pa_reshape_and_cache", "pa_decode_workspace_size", "pa_decode", "pa
             "pa_bm_commit", "pa_bm_fork", "pa_bm_free_request", "pa_bm_get_blocks", "pa_bm_slot_mapping",
             "pa_bm_take_copies", "pa_bm_free_queue", "pa_bm_block_info", "pa_bm_num_blocks_for_memory", "pa_sha256",
             "pa_copy_blocks", "pa_reshape_and_cache_bs", "pa_decode_bs", "pa_prefill_chunk_bs",
-            "pa_copy_blocks_bs")
+            "pa_copy_blocks_bs", "pa_step")
 #: block sizes the *_bs entry points accept
 BLOCK_SIZES = (16, 32, 64, 128)
 #: size of the library's fixed scratch used by pa_decode_noalloc
@@ -33,6 +33,28 @@ PA_DECODE_NOALLOC_MAX_BYTES = 16 * 1024 * 1024
 
 _lock = threading.Lock()
 _lib = None
+
+
+class StepDesc(ctypes.Structure):
+    """Mirror of pa_step_desc in include/pa.h (same fields, same order, C layout)."""
+    _fields_ = [
+        ("k_cache", ctypes.c_void_p), ("v_cache", ctypes.c_void_p),
+        ("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+        ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+        ("scale", ctypes.c_float), ("dtype", ctypes.c_int),
+        ("k_new", ctypes.c_void_p), ("v_new", ctypes.c_void_p), ("slot_mapping", ctypes.c_void_p),
+        ("num_new_tokens", ctypes.c_int32),
+        ("prefill_out", ctypes.c_void_p), ("prefill_q", ctypes.c_void_p), ("prefill_block_table", ctypes.c_void_p),
+        ("prefill_max_blocks_per_seq", ctypes.c_int32), ("prefill_seq_lens", ctypes.c_void_p),
+        ("query_start_loc", ctypes.c_void_p),
+        ("num_prefill_seqs", ctypes.c_int32), ("max_chunk_len", ctypes.c_int32),
+        ("prefill_max_seq_len", ctypes.c_int32),
+        ("decode_out", ctypes.c_void_p), ("decode_q", ctypes.c_void_p), ("decode_block_table", ctypes.c_void_p),
+        ("decode_max_blocks_per_seq", ctypes.c_int32), ("decode_seq_lens", ctypes.c_void_p),
+        ("num_decode_seqs", ctypes.c_int32), ("decode_max_seq_len", ctypes.c_int32),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("decode_sms", ctypes.c_int32), ("timing_events", ctypes.c_void_p),
+    ]
 
 
 class PaError(RuntimeError):
@@ -91,7 +113,8 @@ def load(build_if_needed: bool = True) -> ctypes.CDLL:
                                                     f32, ctypes.c_int, vp, sz, vp]),
                     ("pa_prefill_chunk_bs", ctypes.c_int, [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32,
                                                            i32, i32, i32, f32, ctypes.c_int, vp]),
-                    ("pa_copy_blocks_bs", ctypes.c_int, [vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_int, vp])):
+                    ("pa_copy_blocks_bs", ctypes.c_int, [vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_int, vp]),
+                    ("pa_step", ctypes.c_int, [ctypes.POINTER(StepDesc), vp])):
                 fn = getattr(lib, name)
                 fn.restype = res
                 fn.argtypes = args
@@ -267,6 +290,53 @@ def pa_copy_blocks(k_cache, v_cache, block_pairs, stream=None, _bs: bool = False
 def pa_copy_blocks_bs(k_cache, v_cache, block_pairs, stream=None) -> None:
     """pa_copy_blocks through the block-size entry point (block size = k_cache.shape[2])."""
     pa_copy_blocks(k_cache, v_cache, block_pairs, stream, _bs=True)
+
+
+def pa_step(k_cache, v_cache, scale: float, k_new=None, v_new=None, slot_mapping=None,
+            prefill_out=None, prefill_q=None, prefill_block_table=None, prefill_seq_lens=None, query_start_loc=None,
+            max_chunk_len: int = 0, prefill_max_seq_len: int = 0,
+            decode_out=None, decode_q=None, decode_block_table=None, decode_seq_lens=None,
+            decode_max_seq_len: int = 0, workspace=None, decode_sms: int = 0, timing_events=None,
+            stream=None) -> None:
+    """One whole mixed step (C ABI pa_step): reshape_and_cache of the new tokens, then chunked
+    prefill and decode attention side by side. A part whose tensors are None is skipped.
+    k_cache, v_cache: [NB, H_kv, BS, D]; the other tensors as for the single-kernel calls.
+    timing_events: None or six torch.cuda.Event (or None) recorded before/after reshape,
+    prefill and decode on the stream each kernel runs on."""
+    _need_cuda(k_cache, v_cache, k_new, v_new, slot_mapping, prefill_out, prefill_q, prefill_block_table,
+               prefill_seq_lens, query_start_loc, decode_out, decode_q, decode_block_table, decode_seq_lens,
+               workspace)
+    NB, H_kv, BS, D = k_cache.shape
+    q_any = prefill_q if prefill_q is not None else decode_q
+    d = StepDesc()
+    d.k_cache, d.v_cache = _ptr(k_cache), _ptr(v_cache)
+    d.num_blocks, d.block_size, d.num_kv_heads, d.head_dim = NB, BS, H_kv, D
+    d.num_q_heads = q_any.shape[1] if q_any is not None else H_kv
+    d.scale, d.dtype = float(scale), _dtype_code(k_cache)
+    if slot_mapping is not None:
+        d.k_new, d.v_new, d.slot_mapping = _ptr(k_new), _ptr(v_new), _ptr(slot_mapping)
+        d.num_new_tokens = slot_mapping.shape[0]
+    if prefill_q is not None:
+        d.prefill_out, d.prefill_q = _ptr(prefill_out), _ptr(prefill_q)
+        d.prefill_block_table, d.prefill_max_blocks_per_seq = _ptr(prefill_block_table), prefill_block_table.shape[1]
+        d.prefill_seq_lens, d.query_start_loc = _ptr(prefill_seq_lens), _ptr(query_start_loc)
+        d.num_prefill_seqs = prefill_seq_lens.shape[0]
+        d.max_chunk_len, d.prefill_max_seq_len = int(max_chunk_len), int(prefill_max_seq_len)
+    if decode_q is not None:
+        d.decode_out, d.decode_q = _ptr(decode_out), _ptr(decode_q)
+        d.decode_block_table, d.decode_max_blocks_per_seq = _ptr(decode_block_table), decode_block_table.shape[1]
+        d.decode_seq_lens, d.num_decode_seqs = _ptr(decode_seq_lens), decode_seq_lens.shape[0]
+        d.decode_max_seq_len = int(decode_max_seq_len)
+    if workspace is not None:
+        d.workspace, d.workspace_bytes = _ptr(workspace), workspace.numel() * workspace.element_size()
+    d.decode_sms = int(decode_sms)
+    evs = None
+    if timing_events is not None:
+        if any(e is not None and not e.cuda_event for e in timing_events):
+            raise ValueError("record each timing event once before passing it (torch creates events lazily)")
+        evs = (ctypes.c_void_p * 6)(*[None if e is None else e.cuda_event for e in timing_events])
+        d.timing_events = ctypes.cast(evs, ctypes.c_void_p)
+    _check("pa_step", load().pa_step(ctypes.byref(d), _stream(stream)))
 
 
 def pa_sha256(data: bytes) -> bytes:

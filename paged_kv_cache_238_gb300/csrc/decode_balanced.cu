@@ -814,7 +814,8 @@ int ctas_per_sm(uint32_t smem) {
 
 }  // namespace
 
-bool plan_decode_balanced(int32_t S, int32_t Hkv, int32_t G, int32_t D, const DeviceInfo& dev, DecodePlan* plan) {
+bool plan_decode_balanced(int32_t S, int32_t Hkv, int32_t G, int32_t D, const DeviceInfo& dev, DecodePlan* plan,
+                          int32_t max_ctas) {
     if (G < 4 || G > kBalMaxGroup || (D != 64 && D != 128) || S > kBalMaxSeqs || S < 1) return false;
     const uint32_t stage = bal_stage_bytes(D, G);
     // Prefer 8 streaming warps per CTA with as many stages as fit; 4 warps for large groups.
@@ -831,6 +832,7 @@ bool plan_decode_balanced(int32_t S, int32_t Hkv, int32_t G, int32_t D, const De
             plan->stage_bytes = stage;
             plan->smem_bytes = L.total;
             plan->num_ctas = dev.num_sms * per_sm;
+            if (max_ctas > 0 && plan->num_ctas > max_ctas) plan->num_ctas = max_ctas;
             plan->workspace_bytes = bal_ws_bytes(S, Hkv, G, D, plan->num_ctas);
             return true;
         }

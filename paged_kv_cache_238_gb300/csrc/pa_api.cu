@@ -24,10 +24,15 @@ struct DeviceCache {
     bool ready;
     DeviceInfo info;
     uint32_t* err;  // device address of g_device_errors on this device
+    // pa_step's fork/join: a non-blocking side stream and two events (no timing), created with
+    // the cache entry and kept until the process exits
+    cudaStream_t side;
+    cudaEvent_t fork, join;
 };
 
 DeviceCache g_devices[kMaxDevices];
 std::mutex g_mutex;
+std::mutex g_step_mutex;  // one fork/join at a time per process
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
 
@@ -48,6 +53,18 @@ cudaError_t device_cache(DeviceCache** out) {
         void* err = nullptr;
         e = cudaGetSymbolAddress(&err, g_device_errors);
         if (e != cudaSuccess) return e;
+        if (!c.side) {
+            e = cudaStreamCreateWithFlags(&c.side, cudaStreamNonBlocking);
+            if (e != cudaSuccess) return e;
+        }
+        if (!c.fork) {
+            e = cudaEventCreateWithFlags(&c.fork, cudaEventDisableTiming);
+            if (e != cudaSuccess) return e;
+        }
+        if (!c.join) {
+            e = cudaEventCreateWithFlags(&c.join, cudaEventDisableTiming);
+            if (e != cudaSuccess) return e;
+        }
         c.info = info;
         c.err = static_cast<uint32_t*>(err);
         c.ready = true;
@@ -131,6 +148,89 @@ cudaError_t encode_bf16_3d_sw128(void* map, const void* base, uint64_t d0, uint6
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+
+namespace {
+
+// ------------------------------------------------------------------------------------------
+// argument checks shared by the single-kernel entry points and pa_step
+// ------------------------------------------------------------------------------------------
+pa_status prepare_reshape(const void* k, const void* v, void* k_cache, void* v_cache, const int64_t* slot_mapping,
+                          int32_t num_tokens, int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
+                          int32_t block_size, pa_dtype dtype, ReshapeArgs* a) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0) return PA_ERR_INVALID_ARG;
+    if (!block_size_ok(block_size)) return block_size > 0 ? PA_ERR_UNSUPPORTED : PA_ERR_INVALID_ARG;
+    if (!dtype_ok(dtype)) return PA_ERR_INVALID_ARG;
+    if ((head_dim * elem_bytes(dtype)) % 16 != 0) return PA_ERR_UNSUPPORTED;
+    *a = ReshapeArgs{k, v, k_cache, v_cache, slot_mapping, num_tokens, num_kv_heads, head_dim, num_blocks,
+                     elem_bytes(dtype), block_size, nullptr};
+    if (num_tokens == 0) return PA_OK;
+    if (!k || !v || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+        return PA_ERR_INVALID_ARG;
+    const int64_t items = static_cast<int64_t>(num_tokens) * num_kv_heads * (head_dim * elem_bytes(dtype) / 16);
+    if (items > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
+
+// Host checks of a decode call that need no device; plan_checked_decode adds the plan.
+pa_status prepare_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                         const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                         int32_t num_seqs, int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                         int32_t head_dim, int32_t num_blocks, int32_t block_size, float scale, pa_dtype dtype,
+                         void* workspace, size_t workspace_bytes, DecodeArgs* a) {
+    pa_status st = check_attention_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks,
+                                         max_blocks_per_seq, max_seq_len, dtype, block_size);
+    if (st != PA_OK) return st;
+    *a = DecodeArgs{out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
+                    num_q_heads, num_kv_heads, head_dim, num_blocks, scale, dtype, workspace, workspace_bytes,
+                    nullptr, block_size};
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_table || !seq_lens) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+        return PA_ERR_INVALID_ARG;
+    return PA_OK;
+}
+
+// The decode plan for a checked call (max_ctas > 0 caps the persistent grid) and the check
+// of the workspace against it.
+pa_status plan_checked_decode(const DecodeArgs& a, const DeviceInfo& info, int32_t max_ctas, DecodePlan* plan) {
+    *plan = plan_decode(a.num_seqs, a.num_q_heads, a.num_kv_heads, a.head_dim, a.max_seq_len, a.dtype, info,
+                        max_ctas);
+    if (plan->workspace_bytes > 0 &&
+        (!a.workspace || a.workspace_bytes < plan->workspace_bytes || !aligned16(a.workspace)))
+        return PA_ERR_INVALID_ARG;
+    return PA_OK;
+}
+
+pa_status prepare_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                          const int32_t* query_start_loc, int32_t num_seqs, int32_t max_chunk_len,
+                          int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                          int32_t num_blocks, int32_t block_size, float scale, pa_dtype dtype, PrefillArgs* a) {
+    pa_status st = check_attention_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks,
+                                         max_blocks_per_seq, max_seq_len, dtype, block_size);
+    if (st != PA_OK) return st;
+    if (max_chunk_len < 0 || max_chunk_len > max_seq_len) return PA_ERR_INVALID_ARG;
+    *a = PrefillArgs{out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens, query_start_loc, num_seqs,
+                     max_chunk_len, max_seq_len, num_q_heads, num_kv_heads, head_dim, num_blocks, scale, dtype,
+                     nullptr, block_size};
+    if (num_seqs == 0 || max_chunk_len == 0) return PA_OK;
+    if (static_cast<int64_t>(num_seqs) * max_chunk_len > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    if (!out || !q || !k_cache || !v_cache || !block_table || !seq_lens || !query_start_loc)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
+        (reinterpret_cast<uintptr_t>(query_start_loc) & 3u))
+        return PA_ERR_INVALID_ARG;
+    return PA_OK;
+}
+
+bool prefill_has_work(const PrefillArgs& a) { return a.num_seqs > 0 && a.max_chunk_len > 0; }
+
+}  // namespace
+
 }  // namespace pa
 
 using namespace pa;
@@ -152,21 +252,13 @@ PA_API pa_status pa_reshape_and_cache_bs(const void* k, const void* v, void* k_c
                                          const int64_t* slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
                                          int32_t head_dim, int32_t num_blocks, int32_t block_size, pa_dtype dtype,
                                          void* stream) {
-    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0) return PA_ERR_INVALID_ARG;
-    if (!block_size_ok(block_size)) return block_size > 0 ? PA_ERR_UNSUPPORTED : PA_ERR_INVALID_ARG;
-    if (!dtype_ok(dtype)) return PA_ERR_INVALID_ARG;
-    if ((head_dim * elem_bytes(dtype)) % 16 != 0) return PA_ERR_UNSUPPORTED;
-    if (num_tokens == 0) return PA_OK;
-    if (!k || !v || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
-    if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) ||
-        (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
-        return PA_ERR_INVALID_ARG;
-    const int64_t items = static_cast<int64_t>(num_tokens) * num_kv_heads * (head_dim * elem_bytes(dtype) / 16);
-    if (items > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+    ReshapeArgs a;
+    pa_status st = prepare_reshape(k, v, k_cache, v_cache, slot_mapping, num_tokens, num_kv_heads, head_dim,
+                                   num_blocks, block_size, dtype, &a);
+    if (st != PA_OK || num_tokens == 0) return st;
     DeviceCache* dev = nullptr;
     if (device_cache(&dev) != cudaSuccess) return PA_ERR_CUDA;
-    ReshapeArgs a{k, v, k_cache, v_cache, slot_mapping, num_tokens, num_kv_heads, head_dim, num_blocks,
-                  elem_bytes(dtype), block_size, dev->err};
+    a.err = dev->err;
     return launch_reshape_and_cache(a, dev->info.num_sms, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? PA_OK
                : PA_ERR_CUDA;
@@ -223,22 +315,17 @@ PA_API pa_status pa_decode_bs(void* out, const void* q, const void* k_cache, con
                               int32_t num_seqs, int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
                               int32_t head_dim, int32_t num_blocks, int32_t block_size, float scale, pa_dtype dtype,
                               void* workspace, size_t workspace_bytes, void* stream) {
-    pa_status st = check_attention_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks,
-                                         max_blocks_per_seq, max_seq_len, dtype, block_size);
-    if (st != PA_OK) return st;
-    if (num_seqs == 0) return PA_OK;
-    if (!out || !q || !k_cache || !v_cache || !block_table || !seq_lens) return PA_ERR_INVALID_ARG;
-    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
-        (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
-        return PA_ERR_INVALID_ARG;
+    DecodeArgs a;
+    pa_status st = prepare_decode(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens, num_seqs,
+                                  max_seq_len, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale,
+                                  dtype, workspace, workspace_bytes, &a);
+    if (st != PA_OK || num_seqs == 0) return st;
     DeviceCache* dev = nullptr;
     if (device_cache(&dev) != cudaSuccess) return PA_ERR_CUDA;
-    const DecodePlan plan = plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, max_seq_len, dtype, dev->info);
-    if (plan.workspace_bytes > 0 && (!workspace || workspace_bytes < plan.workspace_bytes || !aligned16(workspace)))
-        return PA_ERR_INVALID_ARG;
-    DecodeArgs a{out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens, num_seqs, max_seq_len,
-                 num_q_heads, num_kv_heads, head_dim, num_blocks, scale, dtype, workspace, workspace_bytes,
-                 dev->err, block_size};
+    DecodePlan plan;
+    st = plan_checked_decode(a, dev->info, 0, &plan);
+    if (st != PA_OK) return st;
+    a.err = dev->err;
     return launch_decode(a, plan, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -258,23 +345,14 @@ PA_API pa_status pa_prefill_chunk_bs(void* out, const void* q, const void* k_cac
                                      int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
                                      int32_t head_dim, int32_t num_blocks, int32_t block_size, float scale,
                                      pa_dtype dtype, void* stream) {
-    pa_status st = check_attention_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks,
-                                         max_blocks_per_seq, max_seq_len, dtype, block_size);
-    if (st != PA_OK) return st;
-    if (max_chunk_len < 0 || max_chunk_len > max_seq_len) return PA_ERR_INVALID_ARG;
-    if (num_seqs == 0 || max_chunk_len == 0) return PA_OK;
-    if (static_cast<int64_t>(num_seqs) * max_chunk_len > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
-    if (!out || !q || !k_cache || !v_cache || !block_table || !seq_lens || !query_start_loc)
-        return PA_ERR_INVALID_ARG;
-    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
-        (reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
-        (reinterpret_cast<uintptr_t>(query_start_loc) & 3u))
-        return PA_ERR_INVALID_ARG;
+    PrefillArgs a;
+    pa_status st = prepare_prefill(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens,
+                                   query_start_loc, num_seqs, max_chunk_len, max_seq_len, num_q_heads, num_kv_heads,
+                                   head_dim, num_blocks, block_size, scale, dtype, &a);
+    if (st != PA_OK || !prefill_has_work(a)) return st;
     DeviceCache* dev = nullptr;
     if (device_cache(&dev) != cudaSuccess) return PA_ERR_CUDA;
-    PrefillArgs a{out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens, query_start_loc, num_seqs,
-                  max_chunk_len, max_seq_len, num_q_heads, num_kv_heads, head_dim, num_blocks, scale, dtype,
-                  dev->err, block_size};
+    a.err = dev->err;
     return launch_prefill(a, dev->info, static_cast<cudaStream_t>(stream)) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -287,6 +365,85 @@ PA_API pa_status pa_prefill_chunk(void* out, const void* q, const void* k_cache,
     return pa_prefill_chunk_bs(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens, query_start_loc,
                                num_seqs, max_chunk_len, max_seq_len, num_q_heads, num_kv_heads, head_dim, num_blocks,
                                PA_BLOCK_SIZE, scale, dtype, stream);
+}
+
+PA_API pa_status pa_step(const pa_step_desc* d, void* stream_ptr) {
+    if (!d) return PA_ERR_INVALID_ARG;
+    if (d->decode_sms < 0 || d->num_new_tokens < 0 || d->num_prefill_seqs < 0 || d->num_decode_seqs < 0)
+        return PA_ERR_INVALID_ARG;
+    // Each part with work is checked as its own entry point would check it; parts without work
+    // are skipped whole (their pointers and sizes may be zero).
+    const bool has_new = d->num_new_tokens > 0, has_dec = d->num_decode_seqs > 0;
+    ReshapeArgs ra{};
+    PrefillArgs pa_{};
+    DecodeArgs da{};
+    pa_status st = PA_OK;
+    if (has_new) {
+        st = prepare_reshape(d->k_new, d->v_new, d->k_cache, d->v_cache, d->slot_mapping, d->num_new_tokens,
+                             d->num_kv_heads, d->head_dim, d->num_blocks, d->block_size, d->dtype, &ra);
+        if (st != PA_OK) return st;
+    }
+    if (d->num_prefill_seqs > 0) {
+        st = prepare_prefill(d->prefill_out, d->prefill_q, d->k_cache, d->v_cache, d->prefill_block_table,
+                             d->prefill_max_blocks_per_seq, d->prefill_seq_lens, d->query_start_loc,
+                             d->num_prefill_seqs, d->max_chunk_len, d->prefill_max_seq_len, d->num_q_heads,
+                             d->num_kv_heads, d->head_dim, d->num_blocks, d->block_size, d->scale, d->dtype, &pa_);
+        if (st != PA_OK) return st;
+    }
+    if (has_dec) {
+        st = prepare_decode(d->decode_out, d->decode_q, d->k_cache, d->v_cache, d->decode_block_table,
+                            d->decode_max_blocks_per_seq, d->decode_seq_lens, d->num_decode_seqs,
+                            d->decode_max_seq_len, d->num_q_heads, d->num_kv_heads, d->head_dim, d->num_blocks,
+                            d->block_size, d->scale, d->dtype, d->workspace, d->workspace_bytes, &da);
+        if (st != PA_OK) return st;
+    }
+    const bool has_pre = d->num_prefill_seqs > 0 && prefill_has_work(pa_);
+    if (!has_new && !has_pre && !has_dec) return PA_OK;
+    DeviceCache* dev = nullptr;
+    if (device_cache(&dev) != cudaSuccess) return PA_ERR_CUDA;
+    DecodePlan plan{};
+    if (has_dec) {
+        const int32_t n = dev->info.num_sms;
+        const int32_t sms = d->decode_sms == 0 ? (n + 1) / 2 : (d->decode_sms < n ? d->decode_sms : n);
+        st = plan_checked_decode(da, dev->info, has_pre ? sms : 0, &plan);
+        if (st != PA_OK) return st;
+    }
+    ra.err = pa_.err = da.err = dev->err;
+    cudaStream_t s = static_cast<cudaStream_t>(stream_ptr);
+    void* const* ev = d->timing_events;
+    // The caller's timing events become event-record nodes when the stream is being captured
+    // (the external flag is valid only under capture).
+    auto mark = [&](int i, cudaStream_t on) -> bool {
+        if (!ev || !ev[i]) return true;
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(on, &cs) != cudaSuccess) return false;
+        const unsigned flags = cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
+        return cudaEventRecordWithFlags(static_cast<cudaEvent_t>(ev[i]), on, flags) == cudaSuccess;
+    };
+    if (has_new) {
+        if (!mark(0, s) || launch_reshape_and_cache(ra, dev->info.num_sms, s) != cudaSuccess || !mark(1, s))
+            return PA_ERR_CUDA;
+    }
+    const bool side_by_side = has_pre && has_dec && plan.path == kDecodeMmaBalanced;
+    if (!side_by_side) {
+        if (has_pre && (!mark(2, s) || launch_prefill(pa_, dev->info, s) != cudaSuccess || !mark(3, s)))
+            return PA_ERR_CUDA;
+        if (has_dec && (!mark(4, s) || launch_decode(da, plan, s) != cudaSuccess || !mark(5, s)))
+            return PA_ERR_CUDA;
+        return PA_OK;
+    }
+    // Fork: the side stream waits for the new tokens; the decode grid is launched first so its
+    // persistent CTAs take their SMs before the prefill grid fills the rest.
+    std::lock_guard<std::mutex> lock(g_step_mutex);
+    if (cudaEventRecord(dev->fork, s) != cudaSuccess) return PA_ERR_CUDA;
+    if (!mark(4, s) || launch_decode(da, plan, s) != cudaSuccess || !mark(5, s)) return PA_ERR_CUDA;
+    if (cudaStreamWaitEvent(dev->side, dev->fork, 0) != cudaSuccess) return PA_ERR_CUDA;
+    if (!mark(2, dev->side) || launch_prefill(pa_, dev->info, dev->side) != cudaSuccess || !mark(3, dev->side))
+        return PA_ERR_CUDA;
+    // Join: later work on `stream` waits for the prefill too.
+    if (cudaEventRecord(dev->join, dev->side) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaStreamWaitEvent(s, dev->join, 0) != cudaSuccess) return PA_ERR_CUDA;
+    return PA_OK;
 }
 
 PA_API pa_status pa_get_device_errors(uint32_t* errors, int32_t clear) {

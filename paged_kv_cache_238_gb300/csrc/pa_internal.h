@@ -92,14 +92,16 @@ struct DeviceInfo {
 // Fills `info` for the current device (cached per device after the first call).
 cudaError_t current_device_info(DeviceInfo* info);
 
+// max_ctas > 0 caps the persistent grid of the balanced path (the SMs it may hold while
+// another kernel runs beside it); the workspace never grows with a smaller grid.
 DecodePlan plan_decode(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                       int32_t max_seq_len, pa_dtype dtype, const DeviceInfo& dev);
+                       int32_t max_seq_len, pa_dtype dtype, const DeviceInfo& dev, int32_t max_ctas = 0);
 cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream);
 
 // Balanced bf16 path (decode_balanced.cu): fills `plan` and returns true when the shape is
 // eligible (GQA group 4..16, head_dim 64/128, at most 1024 sequences) and fits the device.
 bool plan_decode_balanced(int32_t num_seqs, int32_t num_kv_heads, int32_t group, int32_t head_dim,
-                          const DeviceInfo& dev, DecodePlan* plan);
+                          const DeviceInfo& dev, DecodePlan* plan, int32_t max_ctas = 0);
 cudaError_t launch_decode_balanced(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream);
 
 // SIMT path (decode_simt.cu).

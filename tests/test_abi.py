@@ -164,3 +164,59 @@ def test_other_bs_entry_points_check_the_block_size(bs, expect):
     assert lib.pa_copy_blocks_bs(FAKE, FAKE, FAKE, 2, 2, 128, 8, bs, B.PA_BF16, None) == expect
     assert lib.pa_prefill_chunk_bs(FAKE, FAKE, FAKE, FAKE, FAKE, 4, FAKE, FAKE, 2, 16, 64, 8, 2, 128, 16, bs, 0.1,
                                    B.PA_BF16, None) == expect
+
+
+def test_step_desc_layout_matches_the_header(tmp_path):
+    """The binding's ctypes mirror of pa_step_desc has the C layout (offsets from gcc)."""
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("needs gcc")
+    names = [f[0] for f in B.StepDesc._fields_]
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "pa.h"\nint main(void) {\n'
+                   '  printf("%zu\\n", sizeof(pa_step_desc));\n' +
+                   "".join(f'  printf("%zu\\n", offsetof(pa_step_desc, {n}));\n' for n in names) + "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    import subprocess
+    subprocess.run([gcc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    want = [ctypes.sizeof(B.StepDesc)] + [getattr(B.StepDesc, n).offset for n in names]
+    assert got == want
+
+
+def _step(**kw):
+    d = B.StepDesc()
+    base = dict(k_cache=FAKE, v_cache=FAKE, num_blocks=64, block_size=16, num_q_heads=8, num_kv_heads=2,
+                head_dim=128, scale=0.1, dtype=B.PA_BF16,
+                decode_out=FAKE, decode_q=FAKE, decode_block_table=FAKE, decode_max_blocks_per_seq=4,
+                decode_seq_lens=FAKE, num_decode_seqs=2, decode_max_seq_len=64, workspace=FAKE,
+                workspace_bytes=1 << 24,
+                prefill_out=FAKE, prefill_q=FAKE, prefill_block_table=FAKE, prefill_max_blocks_per_seq=4,
+                prefill_seq_lens=FAKE, query_start_loc=FAKE, num_prefill_seqs=2, max_chunk_len=16,
+                prefill_max_seq_len=64, k_new=FAKE, v_new=FAKE, slot_mapping=FAKE, num_new_tokens=4)
+    base.update(kw)
+    for k, v in base.items():
+        setattr(d, k, v)
+    return B.load().pa_step(ctypes.byref(d), None)
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(decode_sms=-1), B.PA_ERR_INVALID_ARG),
+    (dict(num_decode_seqs=-1), B.PA_ERR_INVALID_ARG),
+    (dict(head_dim=96), B.PA_ERR_UNSUPPORTED),
+    (dict(block_size=48), B.PA_ERR_UNSUPPORTED),
+    (dict(num_q_heads=6, num_kv_heads=4), B.PA_ERR_INVALID_ARG),
+    (dict(decode_q=None), B.PA_ERR_INVALID_ARG),                 # a part's own checks still apply
+    (dict(query_start_loc=None), B.PA_ERR_INVALID_ARG),
+    (dict(slot_mapping=FAKE + 4), B.PA_ERR_INVALID_ARG),
+    (dict(prefill_max_seq_len=65), B.PA_ERR_INVALID_ARG),        # beyond 4 blocks of 16
+    (dict(num_new_tokens=0, num_prefill_seqs=0, num_decode_seqs=0, k_cache=None), B.PA_OK),  # nothing to do
+    (dict(num_new_tokens=0, num_prefill_seqs=0, num_decode_seqs=0, prefill_max_blocks_per_seq=0,
+          decode_max_blocks_per_seq=0), B.PA_OK),              # skipped parts are not checked
+])
+def test_step_rejects_bad_arguments(kw, expect):
+    assert _step(**kw) == expect
+
+
+def test_step_null_descriptor():
+    assert B.load().pa_step(None, None) == B.PA_ERR_INVALID_ARG
