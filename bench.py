@@ -393,8 +393,38 @@ class DeviceStep:
             self.outputs.append(self.outp)
         self.kernels = [k for k, on in (("reshape", self.has_new), ("prefill", self.has_pre),
                                         ("decode", self.has_dec)) if on]
+        # The step's inputs (and its outputs) live in one device arena each, so the end-to-end
+        # step moves them with one host->device and one device->host copy.
+        in_names = [n for n, on in (("k_new", self.has_new), ("v_new", self.has_new), ("slots", self.has_new),
+                                    ("q", self.has_dec), ("bt", self.has_dec), ("lens", self.has_dec),
+                                    ("qp", self.has_pre), ("btp", self.has_pre), ("lp", self.has_pre),
+                                    ("qsl", self.has_pre)) if on]
+        out_names = [n for n, on in (("out", self.has_dec), ("outp", self.has_pre)) if on]
+        self.in_arena = self._pack(in_names, dev, copy=True)
+        self.out_arena = self._pack(out_names, dev, copy=False)
+        self.inputs = [getattr(self, n) for n in in_names]
+        self.outputs = [getattr(self, n) for n in out_names]
         # whole step through pa_step: prefill and decode side by side on an SM split
         self.whole_step = whole_step and self.has_pre and self.has_dec
+
+    def _pack(self, names, dev, copy: bool):
+        """Re-home the named tensors as 256-byte-aligned views of one uint8 device buffer."""
+        import torch
+        if not names:
+            return None
+        offs, total = [], 0
+        for n in names:
+            offs.append(total)
+            t = getattr(self, n)
+            total += -(-t.numel() * t.element_size() // 256) * 256
+        arena = torch.zeros(total, dtype=torch.uint8, device=dev)
+        for n, o in zip(names, offs):
+            t = getattr(self, n)
+            v = arena[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+            if copy:
+                v.copy_(t)
+            setattr(self, n, v)
+        return arena
 
     def __call__(self, i: int, ev=None):
         """Step i on pool i % R; ev maps a kernel name to an event pair recorded around it."""
@@ -507,17 +537,17 @@ def run_ours(args):
     n_main = K // chunk
 
     # ---- e2e graph: pinned host inputs in, results out, every step ------------------------
-    h_in = [t.cpu().pin_memory() for t in step.inputs]
-    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in step.outputs]
-    h2d = sum(t.numel() * t.element_size() for t in h_in)
-    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    # the step's inputs and outputs are packed in one device buffer each (DeviceStep), so a
+    # step moves them with one copy each way
+    h_in = step.in_arena.cpu().pin_memory()
+    h_out = torch.empty(step.out_arena.shape, dtype=torch.uint8, pin_memory=True)
+    h2d = h_in.numel()
+    d2h = h_out.numel()
 
     def e2e_step(i):
-        for d, h in zip(step.inputs, h_in):
-            d.copy_(h, non_blocking=True)
+        step.in_arena.copy_(h_in, non_blocking=True)
         step(i)
-        for h, d in zip(h_out, step.outputs):
-            h.copy_(d, non_blocking=True)
+        h_out.copy_(step.out_arena, non_blocking=True)
 
     g_e2e = capture(e2e_step, chunk, False)
     g_e2e_rem = capture(e2e_step, rem, False) if rem else None
