@@ -357,7 +357,8 @@ class DeviceStep:
     """The workload's device tensors (R rotated KV pools) and one step of the hot path:
     reshape_and_cache of the step's new tokens, then chunked prefill and decode attention."""
 
-    def __init__(self, wl, dev, R: int, stream, whole_step: bool = False, decode_sms: int = 0):
+    def __init__(self, wl, dev, R: int, stream, whole_step: bool = False, decode_sms: int = 0,
+                 fuse_append: bool = False):
         import torch
         from paged_kv_cache_238_gb300 import binding as B
         self.B, self.wl, self.stream, self.R = B, wl, stream, R
@@ -406,6 +407,11 @@ class DeviceStep:
         self.outputs = [getattr(self, n) for n in out_names]
         # whole step through pa_step: prefill and decode side by side on an SM split
         self.whole_step = whole_step and self.has_pre and self.has_dec
+        # decode-only step with one new token per sequence: pa_decode_append (write + attention)
+        self.fused_append = (fuse_append and self.has_new and self.has_dec and not self.has_pre and
+                             wl.slot_mapping.shape[0] == wl.S)
+        if self.fused_append:
+            self.kernels = ["decode"]
 
     def _pack(self, names, dev, copy: bool):
         """Re-home the named tensors as 256-byte-aligned views of one uint8 device buffer."""
@@ -447,6 +453,12 @@ class DeviceStep:
                       decode_max_seq_len=self.msl, workspace=self.ws, decode_sms=self.decode_sms,
                       timing_events=tev, stream=s)
             return
+        if self.fused_append:
+            rec("decode", 0)
+            B.pa_decode_append(self.out, self.q, self.k_new, self.v_new, self.slots, self.kcs[r], self.vcs[r], self.bt,
+                               self.lens, self.msl, wl.scale, self.ws, stream=s)
+            rec("decode", 1)
+            return
         if self.has_new:
             rec("reshape", 0)
             B.pa_reshape_and_cache(self.k_new, self.v_new, self.kcs[r], self.vcs[r], self.slots, stream=s)
@@ -464,6 +476,7 @@ class DeviceStep:
 
 
 KERNEL_LABEL = {
+    "decode_append": "pa_decode_append: balanced TMA + mma.sync decode with the new tokens' K/V write fused in",
     "decode": "pa_decode: balanced TMA + mma.sync decode kernel (split merge in-kernel)",
     "prefill": "pa_prefill_chunk: tcgen05 chunked-prefill kernel (TMA page gather, S/O/P in TMEM)",
     "reshape": "pa_reshape_and_cache: slot scatter",
@@ -490,7 +503,16 @@ def run_ours(args):
     nbytes = step_bytes(wl)
     R = args.replicas
     stream = torch.cuda.Stream(device=dev)
-    step = DeviceStep(wl, dev, R, stream, whole_step=not args.sequential, decode_sms=args.decode_sms)
+    step = DeviceStep(wl, dev, R, stream, whole_step=not args.sequential, decode_sms=args.decode_sms,
+                      fuse_append=not args.sequential)
+    if step.fused_append:
+        # one kernel writes the new tokens and attends: its algorithmic bytes are the decode's
+        # plus the new rows read once from the input and written once (not read back)
+        new = wl.slot_mapping.shape[0] * _kv_token_bytes(wl)
+        nbytes = dict(nbytes)
+        nbytes["decode"] = nbytes["decode"] + nbytes["reshape"] - new
+        nbytes["step"] = nbytes["step"] - new
+        nbytes["reshape"] = 0
 
     # ---- warm-up (eager, untimed) ----------------------------------------------------------
     with torch.cuda.stream(stream):
@@ -648,6 +670,9 @@ def run_ours(args):
         "gpu_launches": launches_per_step * K,
         "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
     }
+    if step.fused_append:
+        line["config"]["step_call"] = "pa_decode_append: one launch writes the new tokens' K/V and attends"
+        line["roofline"]["kernel"] = KERNEL_LABEL["decode_append"]
     if step.whole_step:
         line["config"]["step_call"] = (f"pa_step: reshape_and_cache, then prefill and decode side by side "
                                        f"(decode on {args.decode_sms or 'half the'} SMs)")
@@ -735,7 +760,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-cupti", action="store_true", help="skip the activity-trace launch count (e.g. under ncu)")
     ap.add_argument("--sequential", action="store_true",
-                    help="mixed step as three separate calls instead of pa_step (prefill beside decode)")
+                    help="one call per kernel: no pa_step (mixed step) and no pa_decode_append (decode step)")
     ap.add_argument("--decode-sms", type=int, default=0, help="pa_step: SMs held by decode (0 = half)")
     args = ap.parse_args(argv)
     _, _, default_steps, default_replicas = WORKLOADS[args.workload]

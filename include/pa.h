@@ -79,6 +79,8 @@ typedef enum {
 #define PA_DEVERR_BLOCK_RANGE  0x2u  /* a block-table entry outside [0, num_blocks)       */
 #define PA_DEVERR_LEN_RANGE    0x4u  /* a length beyond the table row or max_seq_len      */
 #define PA_DEVERR_WAIT_TIMEOUT 0x8u  /* a bounded pipeline wait gave up (results invalid) */
+#define PA_DEVERR_APPEND_SLOT  0x10u /* pa_decode_append: slot_mapping[i] is not the slot the
+                                        block table gives position seq_lens[i] - 1          */
 
 /*
  * pa_reshape_and_cache: write the K/V rows of num_tokens new tokens into their slots.
@@ -159,6 +161,32 @@ PA_API pa_status pa_decode(void* out, const void* q, const void* k_cache, const 
                     int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                     int32_t num_blocks, float scale, pa_dtype dtype,
                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * pa_decode_append: one decode step with its new tokens, in one launch where it can be. For
+ * each sequence i the token at position seq_lens[i] - 1 is new: its K and V rows k_new[i],
+ * v_new[i] ([num_seqs][num_kv_heads][head_dim]) are written to slot slot_mapping[i] of the
+ * pool, exactly as pa_reshape_and_cache_bs writes them, and decode attention runs over keys
+ * 0 .. seq_lens[i] - 1 as pa_decode_bs does. New K/V reach the cache as each token is produced
+ * ("My Understanding of vLLM and PagedAttention", "Step 3 - Tokens Generated Sequentially");
+ * fusing the write into the attention launch is this library's, not the pages'.
+ *
+ * On the bf16 persistent path (GQA groups 4..16) one kernel does both: attention takes the new
+ * rows from k_new / v_new, so it never waits for its own pool writes. Elsewhere the call
+ * launches pa_reshape_and_cache's kernel and then the decode kernel. Either way the results
+ * equal pa_reshape_and_cache_bs followed by pa_decode_bs when slot_mapping[i] is the slot that
+ * block-table row i gives position seq_lens[i] - 1; on the fused path a slot that is not (a
+ * negative one included) sets PA_DEVERR_APPEND_SLOT, the write still goes to slot_mapping[i]
+ * (skipped if negative) and attention uses the new rows at position seq_lens[i] - 1.
+ * Arguments as for pa_decode_bs, plus k_new, v_new (16-byte aligned) and slot_mapping
+ * (int64 [num_seqs], 8-byte aligned); workspace as for pa_decode.
+ */
+PA_API pa_status pa_decode_append(void* out, const void* q, const void* k_new, const void* v_new,
+                                  const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                                  const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                  int32_t num_seqs, int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t num_blocks, int32_t block_size, float scale,
+                                  pa_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
 
 /* pa_decode with block_size (see the block-size variants above). */
 PA_API pa_status pa_decode_bs(void* out, const void* q, const void* k_cache, const void* v_cache,

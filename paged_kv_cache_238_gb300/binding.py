@@ -16,6 +16,7 @@ from . import _build
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_NO_SPACE = 0, 1, 2, 3, 4
 PA_F32, PA_BF16 = 0, 1
 PA_DEVERR_SLOT_RANGE, PA_DEVERR_BLOCK_RANGE, PA_DEVERR_LEN_RANGE, PA_DEVERR_WAIT_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+PA_DEVERR_APPEND_SLOT = 0x10
 BLOCK_SIZE = 16
 
 #: every symbol that include/pa.h declares
@@ -25,7 +26,7 @@ EXPORTED = ("pa_reshape_and_cache", "pa_decode_workspace_size", "pa_decode", "pa
             "pa_bm_commit", "pa_bm_fork", "pa_bm_free_request", "pa_bm_get_blocks", "pa_bm_slot_mapping",
             "pa_bm_take_copies", "pa_bm_free_queue", "pa_bm_block_info", "pa_bm_num_blocks_for_memory", "pa_sha256",
             "pa_copy_blocks", "pa_reshape_and_cache_bs", "pa_decode_bs", "pa_prefill_chunk_bs",
-            "pa_copy_blocks_bs", "pa_step")
+            "pa_copy_blocks_bs", "pa_step", "pa_decode_append")
 #: block sizes the *_bs entry points accept
 BLOCK_SIZES = (16, 32, 64, 128)
 #: size of the library's fixed scratch used by pa_decode_noalloc
@@ -114,7 +115,9 @@ def load(build_if_needed: bool = True) -> ctypes.CDLL:
                     ("pa_prefill_chunk_bs", ctypes.c_int, [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32,
                                                            i32, i32, i32, f32, ctypes.c_int, vp]),
                     ("pa_copy_blocks_bs", ctypes.c_int, [vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_int, vp]),
-                    ("pa_step", ctypes.c_int, [ctypes.POINTER(StepDesc), vp])):
+                    ("pa_step", ctypes.c_int, [ctypes.POINTER(StepDesc), vp]),
+                    ("pa_decode_append", ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32,
+                                                        i32, i32, i32, f32, ctypes.c_int, vp, sz, vp])):
                 fn = getattr(lib, name)
                 fn.restype = res
                 fn.argtypes = args
@@ -220,6 +223,21 @@ def pa_decode_bs(out, q, k_cache, v_cache, block_table, seq_lens, max_seq_len: i
                  workspace=None, stream=None) -> None:
     """pa_decode through the block-size entry point (block size = k_cache.shape[2])."""
     pa_decode(out, q, k_cache, v_cache, block_table, seq_lens, max_seq_len, scale, workspace, stream, _bs=True)
+
+
+def pa_decode_append(out, q, k_new, v_new, slot_mapping, k_cache, v_cache, block_table, seq_lens,
+                     max_seq_len: int, scale: float, workspace=None, stream=None) -> None:
+    """Decode step with its new tokens (C ABI pa_decode_append): k_new, v_new [S, H_kv, D] of
+    sequence i's token at position seq_lens[i] - 1 are written to slot_mapping[i] ([S] int64)
+    and attended to; one launch on the bf16 persistent path."""
+    _need_cuda(out, q, k_new, v_new, slot_mapping, k_cache, v_cache, block_table, seq_lens, workspace)
+    S, H_q, D = q.shape
+    NB, H_kv, BS = k_cache.shape[0], k_cache.shape[1], k_cache.shape[2]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("pa_decode_append", load().pa_decode_append(
+        _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
+        _ptr(block_table), block_table.shape[1], _ptr(seq_lens), S, int(max_seq_len), H_q, H_kv, D, NB, int(BS),
+        float(scale), _dtype_code(q), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def pa_decode_noalloc(out, q, k_cache, v_cache, block_table, seq_lens, max_seq_len: int, scale: float,

@@ -11,10 +11,10 @@
 namespace pa {
 
 DecodePlan plan_decode(int32_t S, int32_t Hq, int32_t Hkv, int32_t D, int32_t max_seq_len, pa_dtype dt,
-                       const DeviceInfo& dev, int32_t max_ctas) {
+                       const DeviceInfo& dev, int32_t max_ctas, bool append) {
     DecodePlan plan{};
     const int32_t G = Hq / Hkv;
-    if (dt == PA_BF16 && plan_decode_balanced(S, Hkv, G, D, dev, &plan, max_ctas)) return plan;
+    if (dt == PA_BF16 && plan_decode_balanced(S, Hkv, G, D, dev, &plan, max_ctas, append)) return plan;
 
     plan.path = kDecodeSimtSplit;
     const int32_t heads = simt_heads_per_cta();

@@ -46,9 +46,13 @@ constexpr int kBalMaxSeqs = 1024;  // per-sequence tables live in shared memory
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-// Stage: K page (D/64 swizzled 2 KB boxes), V page, then the segment's query rows.
-__host__ __device__ inline uint32_t bal_stage_bytes(int D, int G) {
-    return align_up(2u * kPageTokens * D * 2u + static_cast<uint32_t>(G) * D * 2u, 1024u);
+// Stage: K page (D/64 swizzled 2 KB boxes), V page, then the segment's query rows; when the
+// call appends each sequence's new token, then that token's K row, V row, its slot (int64) and
+// the page's pool row (int32).
+__host__ __device__ inline uint32_t bal_append_bytes(int D) { return 4u * D + 16u; }
+__host__ __device__ inline uint32_t bal_stage_bytes(int D, int G, bool append) {
+    return align_up(2u * kPageTokens * D * 2u + static_cast<uint32_t>(G) * D * 2u + (append ? bal_append_bytes(D) : 0u),
+                    1024u);
 }
 
 struct BalLayout {
@@ -143,6 +147,13 @@ struct Walker {
         }
     }
 };
+
+// 8-byte asynchronous copy global -> shared whose completion the mbarrier tracks: the arrive
+// raises the barrier's pending count now and lowers it when the copy has landed.
+__device__ __forceinline__ void async_copy8_tracked(void* smem_dst, const void* src, uint64_t* bar) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(smem_dst)), "l"(src) : "memory");
+    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 
 __device__ __forceinline__ void bulk_copy_g2s(void* smem_dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile(
@@ -256,7 +267,8 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
     __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ block_table,
     int32_t max_blocks, const int32_t* __restrict__ seq_lens, int32_t S, int32_t num_kv_heads, int32_t G,
     int32_t num_blocks, int32_t sub_log2, float scale_log2, int32_t nst, uint32_t stage_bytes, BalWorkspace ws,
-    uint32_t* err) {
+    uint32_t* err, const int4* __restrict__ k_new, const int4* __restrict__ v_new,
+    const int64_t* __restrict__ slot_mapping, int4* __restrict__ k_pool, int4* __restrict__ v_pool) {
     constexpr uint32_t kPage = kPageTokens * D * 2;
     constexpr uint32_t kHalves = D / 64;
     constexpr int KS = D / 16;  // k-steps over head_dim
@@ -327,11 +339,34 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
 
     const int64_t U = prefix[S];
     const int64_t C = gridDim.x;
-    // sequences without keys get zero rows (spread over the CTAs)
+    // Append (k_new != nullptr): sequence i's token at position len_i - 1 is new. The warp that
+    // attends over the page holding that position receives the token's K/V rows with the page,
+    // uses them for that row and writes them to slot_mapping[i]: no kernel waits on its own pool
+    // writes, and the writes cost no load latency on the streaming path.
+    const bool append = k_new != nullptr;
+    constexpr int32_t CPR = D * 2 / 16;  // 16-byte chunks per K or V row
+    const int32_t bs_log2 = sub_log2 + 4;
+    // sequences without keys get zero rows (spread over the CTAs); with append their new rows
+    // are written here
     for (int32_t s = blockIdx.x; s < S; s += gridDim.x) {
         if (lens[s] != 0) continue;
         uint32_t* z = reinterpret_cast<uint32_t*>(out + static_cast<int64_t>(s) * Hq * D);
         for (int32_t i = tid; i < Hq * D / 2; i += NTH) z[i] = 0u;
+        if (append) {
+            const int64_t slot = __ldg(slot_mapping + s);
+            if (slot >= (static_cast<int64_t>(num_blocks) << bs_log2)) {
+                if (tid == 0) raise_error(err, PA_DEVERR_SLOT_RANGE);
+            } else if (slot >= 0) {
+                const int64_t blk = slot >> bs_log2, off = slot - (blk << bs_log2);
+                for (int32_t i = tid; i < num_kv_heads * CPR; i += NTH) {
+                    const int32_t h = i / CPR, c = i - h * CPR;
+                    const int64_t dst = (((blk * num_kv_heads + h) << bs_log2) + off) * CPR + c;
+                    const int64_t src = (static_cast<int64_t>(s) * num_kv_heads + h) * CPR + c;
+                    k_pool[dst] = __ldg(k_new + src);
+                    v_pool[dst] = __ldg(v_new + src);
+                }
+            }
+        }
     }
     const int32_t u0 = static_cast<int32_t>(slice_start(blockIdx.x, U, C));
     const int32_t u1 = static_cast<int32_t>(slice_start(blockIdx.x + 1, U, C));
@@ -379,11 +414,23 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
             }
             const int32_t row = __shfl_sync(0xffffffffu, id_cur, t & 31);
             const bool seg_first = (t == 0) || (wi.j == 0);
+            const bool new_row = append && wi.j == wi.np - 1;  // the page that holds position len - 1
             if (lane == 0 && !*abort_flag) {
                 const int32_t st = t % nst;
                 uint8_t* stage = ring + static_cast<uint32_t>(st) * stage_bytes;
                 const uint32_t qbytes = static_cast<uint32_t>(G) * D * 2u;
-                mbar_arrive_expect_tx(&bars[st], 2u * kPage + (seg_first ? qbytes : 0u));
+                if (new_row) {
+                    // behind the query rows: the token's K row, V row, slot and the page's pool row
+                    uint8_t* ex = stage + 2u * kPage + qbytes;
+                    *reinterpret_cast<int32_t*>(ex + 4u * D + 8u) = row;
+                    async_copy8_tracked(ex + 4u * D, slot_mapping + wi.s, &bars[st]);
+                    const int64_t r = static_cast<int64_t>(wi.s) * num_kv_heads + wi.h;
+                    mbar_arrive_expect_tx(&bars[st], 2u * kPage + (seg_first ? qbytes : 0u) + 4u * D);
+                    bulk_copy_g2s(ex, k_new + r * CPR, D * 2u, &bars[st]);
+                    bulk_copy_g2s(ex + D * 2u, v_new + r * CPR, D * 2u, &bars[st]);
+                } else {
+                    mbar_arrive_expect_tx(&bars[st], 2u * kPage + (seg_first ? qbytes : 0u));
+                }
                 if constexpr (kHalves == 2) {  // both 64-column halves in one box
                     tma_load_3d_hint(stage, &tm_k, 0, row, 0, &bars[st], kv_policy);
                     tma_load_3d_hint(stage + kPage, &tm_v, 0, row, 0, &bars[st], kv_policy);
@@ -464,6 +511,30 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
                     const int32_t hf = c / (rows * 8), rem = c - hf * rows * 8;
                     *reinterpret_cast<int4*>(stage + kPage + hf * 2048u + (ntok + rem / 8) * 128u + (rem % 8) * 16u) =
                         make_int4(0, 0, 0, 0);
+                }
+                __syncwarp();
+            }
+            const bool new_row = append && wc.j == wc.np - 1;
+            if (new_row) {
+                // row ntok - 1 is the new token: take its K/V from the appended rows and write
+                // them to the token's slot
+                const uint8_t* ex = stage + 2u * kPage + static_cast<uint32_t>(G) * D * 2u;
+                const int64_t slot = *reinterpret_cast<const int64_t*>(ex + 4u * D);
+                const int64_t want = *reinterpret_cast<const int32_t*>(ex + 4u * D + 8u) + (ntok - 1);
+                int64_t dst_row = -1;
+                if (slot >= 0 && slot < (static_cast<int64_t>(num_blocks) << bs_log2)) {
+                    const int64_t blk = slot >> bs_log2;
+                    dst_row = ((blk * num_kv_heads + wc.h) << bs_log2) + (slot - (blk << bs_log2));
+                } else if (slot >= 0 && lane == 0) {
+                    raise_error(err, PA_DEVERR_SLOT_RANGE);
+                }
+                if (dst_row != want && lane == 0) raise_error(err, PA_DEVERR_APPEND_SLOT);
+                if (lane < 2 * CPR) {
+                    const int32_t kv = lane / CPR, c = lane - kv * CPR;
+                    const int4 val = *reinterpret_cast<const int4*>(ex + kv * D * 2u + c * 16u);
+                    *reinterpret_cast<int4*>(stage + kv * kPage + (c >> 3) * 2048u +
+                                             sw128_offset(static_cast<uint32_t>(ntok - 1), c & 7u)) = val;
+                    if (dst_row >= 0) (kv ? v_pool : k_pool)[dst_row * CPR + c] = val;
                 }
                 __syncwarp();
             }
@@ -601,7 +672,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
                 }
             }
             __syncwarp();
-            if (ntok < kPageTokens) fence_proxy_async_shared();  // generic writes before the next copy
+            if (ntok < kPageTokens || new_row) fence_proxy_async_shared();  // generic writes before the next copy
             if (t + nst < n) issue(t + nst);
             wc.advance(prefix, lens, S, num_kv_heads);
         }
@@ -797,7 +868,9 @@ cudaError_t launch_impl(const DecodeArgs& a, const DecodePlan& plan, cudaStream_
                               static_cast<const __nv_bfloat16*>(a.q), a.block_table, a.max_blocks_per_seq,
                               a.seq_lens, a.num_seqs, a.num_kv_heads, G, a.num_blocks,
                               block_size_log2(a.block_size) - 4, a.scale * kLog2e, plan.stages, plan.stage_bytes, ws,
-                              a.err);
+                              a.err, static_cast<const int4*>(a.k_new), static_cast<const int4*>(a.v_new),
+                              a.slot_mapping, static_cast<int4*>(const_cast<void*>(a.k_cache)),
+                              static_cast<int4*>(const_cast<void*>(a.v_cache)));
 }
 
 template <int D, int NW>
@@ -815,9 +888,9 @@ int ctas_per_sm(uint32_t smem) {
 }  // namespace
 
 bool plan_decode_balanced(int32_t S, int32_t Hkv, int32_t G, int32_t D, const DeviceInfo& dev, DecodePlan* plan,
-                          int32_t max_ctas) {
+                          int32_t max_ctas, bool append) {
     if (G < 4 || G > kBalMaxGroup || (D != 64 && D != 128) || S > kBalMaxSeqs || S < 1) return false;
-    const uint32_t stage = bal_stage_bytes(D, G);
+    const uint32_t stage = bal_stage_bytes(D, G, append);
     // Prefer 8 streaming warps per CTA with as many stages as fit; 4 warps for large groups.
     for (int NW : {8, 4}) {
         for (int nst = 4; nst >= 2; --nst) {

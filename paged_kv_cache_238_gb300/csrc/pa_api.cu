@@ -195,9 +195,10 @@ pa_status prepare_decode(void* out, const void* q, const void* k_cache, const vo
 
 // The decode plan for a checked call (max_ctas > 0 caps the persistent grid) and the check
 // of the workspace against it.
-pa_status plan_checked_decode(const DecodeArgs& a, const DeviceInfo& info, int32_t max_ctas, DecodePlan* plan) {
+pa_status plan_checked_decode(const DecodeArgs& a, const DeviceInfo& info, int32_t max_ctas, DecodePlan* plan,
+                              bool append = false) {
     *plan = plan_decode(a.num_seqs, a.num_q_heads, a.num_kv_heads, a.head_dim, a.max_seq_len, a.dtype, info,
-                        max_ctas);
+                        max_ctas, append);
     if (plan->workspace_bytes > 0 &&
         (!a.workspace || a.workspace_bytes < plan->workspace_bytes || !aligned16(a.workspace)))
         return PA_ERR_INVALID_ARG;
@@ -308,6 +309,38 @@ PA_API size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, in
     if (device_cache(&dev) != cudaSuccess) return 0;
     return plan_decode(num_seqs, num_q_heads, num_kv_heads, head_dim, max_seq_len, dtype, dev->info)
         .workspace_bytes;
+}
+
+PA_API pa_status pa_decode_append(void* out, const void* q, const void* k_new, const void* v_new,
+                                  const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                                  const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                  int32_t num_seqs, int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                                  int32_t head_dim, int32_t num_blocks, int32_t block_size, float scale,
+                                  pa_dtype dtype, void* workspace, size_t workspace_bytes, void* stream) {
+    DecodeArgs a;
+    pa_status st = prepare_decode(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens, num_seqs,
+                                  max_seq_len, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale,
+                                  dtype, workspace, workspace_bytes, &a);
+    if (st != PA_OK) return st;
+    ReshapeArgs ra;
+    st = prepare_reshape(k_new, v_new, k_cache, v_cache, slot_mapping, num_seqs, num_kv_heads, head_dim, num_blocks,
+                         block_size, dtype, &ra);
+    if (st != PA_OK || num_seqs == 0) return st;
+    DeviceCache* dev = nullptr;
+    if (device_cache(&dev) != cudaSuccess) return PA_ERR_CUDA;
+    DecodePlan plan;
+    st = plan_checked_decode(a, dev->info, 0, &plan, true);
+    if (st != PA_OK) return st;
+    a.err = ra.err = dev->err;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (plan.path == kDecodeMmaBalanced) {  // one launch: writes and attention
+        a.k_new = k_new;
+        a.v_new = v_new;
+        a.slot_mapping = slot_mapping;
+        return launch_decode(a, plan, s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    }
+    if (launch_reshape_and_cache(ra, dev->info.num_sms, s) != cudaSuccess) return PA_ERR_CUDA;
+    return launch_decode(a, plan, s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 PA_API pa_status pa_decode_bs(void* out, const void* q, const void* k_cache, const void* v_cache,

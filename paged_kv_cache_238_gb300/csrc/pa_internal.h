@@ -63,6 +63,11 @@ struct DecodeArgs {
     size_t workspace_bytes;
     uint32_t* err;
     int32_t block_size;  // tokens per block: 16, 32, 64 or 128
+    // append (balanced path only; null otherwise): sequence i's new token at position
+    // seq_lens[i] - 1, rows [num_seqs][num_kv_heads][head_dim], written to slot_mapping[i]
+    const void* k_new = nullptr;
+    const void* v_new = nullptr;
+    const int64_t* slot_mapping = nullptr;
 };
 
 enum DecodePath : int {
@@ -94,14 +99,16 @@ cudaError_t current_device_info(DeviceInfo* info);
 
 // max_ctas > 0 caps the persistent grid of the balanced path (the SMs it may hold while
 // another kernel runs beside it); the workspace never grows with a smaller grid.
+// append: the balanced path's stages also carry the appended token's rows.
 DecodePlan plan_decode(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                       int32_t max_seq_len, pa_dtype dtype, const DeviceInfo& dev, int32_t max_ctas = 0);
+                       int32_t max_seq_len, pa_dtype dtype, const DeviceInfo& dev, int32_t max_ctas = 0,
+                       bool append = false);
 cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream);
 
 // Balanced bf16 path (decode_balanced.cu): fills `plan` and returns true when the shape is
 // eligible (GQA group 4..16, head_dim 64/128, at most 1024 sequences) and fits the device.
 bool plan_decode_balanced(int32_t num_seqs, int32_t num_kv_heads, int32_t group, int32_t head_dim,
-                          const DeviceInfo& dev, DecodePlan* plan, int32_t max_ctas = 0);
+                          const DeviceInfo& dev, DecodePlan* plan, int32_t max_ctas = 0, bool append = false);
 cudaError_t launch_decode_balanced(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream);
 
 // SIMT path (decode_simt.cu).

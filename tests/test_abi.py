@@ -220,3 +220,21 @@ def test_step_rejects_bad_arguments(kw, expect):
 
 def test_step_null_descriptor():
     assert B.load().pa_step(None, None) == B.PA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(k_new=None), B.PA_ERR_INVALID_ARG),
+    (dict(slots=FAKE + 4), B.PA_ERR_INVALID_ARG),       # int64 slots must be 8-byte aligned
+    (dict(v_new=FAKE + 8), B.PA_ERR_INVALID_ARG),
+    (dict(bs=48), B.PA_ERR_UNSUPPORTED),
+    (dict(D=96), B.PA_ERR_UNSUPPORTED),
+    (dict(max_len=65), B.PA_ERR_INVALID_ARG),
+    (dict(S=0, out=None, q=None, k_new=None), B.PA_OK),
+])
+def test_decode_append_rejects_bad_arguments(kw, expect):
+    a = dict(out=FAKE, q=FAKE, k_new=FAKE, v_new=FAKE, slots=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, mb=4, lens=FAKE, S=2,
+             max_len=64, Hq=8, Hkv=2, D=128, NB=16, bs=16, dt=B.PA_BF16)
+    a.update(kw)
+    assert B.load().pa_decode_append(a["out"], a["q"], a["k_new"], a["v_new"], a["slots"], a["kc"], a["vc"], a["bt"],
+                                     a["mb"], a["lens"], a["S"], a["max_len"], a["Hq"], a["Hkv"], a["D"], a["NB"],
+                                     a["bs"], 0.1, a["dt"], FAKE, 1 << 24, None) == expect
