@@ -371,6 +371,11 @@ typedef struct pa_block_manager pa_block_manager;
  * hash_seed NULL = "paged-kv-none-hash". Free with pa_bm_destroy. */
 PA_API pa_status pa_bm_create(int32_t num_blocks, int32_t enable_caching, const char* hash_seed,
                               pa_block_manager** out);
+/* The same for blocks of block_size tokens (16, 32, 64 or 128; another positive size returns
+ * PA_ERR_UNSUPPORTED): every "16" in the descriptions below reads block_size (hash input,
+ * prefix-hit cap, slots). */
+PA_API pa_status pa_bm_create_bs(int32_t num_blocks, int32_t block_size, int32_t enable_caching,
+                                 const char* hash_seed, pa_block_manager** out);
 PA_API void pa_bm_destroy(pa_block_manager* bm);
 /* Blocks in the free queue (cached-but-free blocks included); -1 for a NULL manager. */
 PA_API int32_t pa_bm_num_free_blocks(const pa_block_manager* bm);
@@ -413,6 +418,10 @@ PA_API pa_status pa_bm_block_info(const pa_block_manager* bm, int32_t block_id, 
  * is sized once from a utilisation fraction of free memory); -1 on a bad argument. */
 PA_API int64_t pa_bm_num_blocks_for_memory(size_t free_bytes, double utilization, int32_t num_layers,
                                            int32_t num_kv_heads, int32_t head_dim, pa_dtype dtype);
+/* The same for blocks of block_size tokens (16, 32, 64 or 128; -1 otherwise). */
+PA_API int64_t pa_bm_num_blocks_for_memory_bs(size_t free_bytes, double utilization, int32_t num_layers,
+                                              int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                              pa_dtype dtype);
 /* SHA-256 (FIPS 180-4) of n bytes, as the block hashes use it. */
 PA_API pa_status pa_sha256(const uint8_t* data, size_t n, uint8_t* out32);
 

@@ -4,8 +4,9 @@ TEST INFRASTRUCTURE ONLY. Nothing on the product path may import or call this mo
 the tests do. It shares no code with the C++ block manager in the library.
 
 What it models (the pages on vLLM's paged KV cache):
-  * A pool of fixed 16-token physical blocks; a request reaches its blocks through a block
-    list, and a slot is physical_block * 16 + offset ("My Understanding of vLLM and
+  * A pool of fixed-size physical blocks (16 tokens by default; "vLLM: what PagedAttention
+    turned into" reports 16 to 128 performing alike, so 32, 64 and 128 are variants); a
+    request reaches its blocks through a block list, and a slot is physical_block * size + offset ("My Understanding of vLLM and
     PagedAttention", "Logical Blocks", "Physical Blocks", "Block Table"; "vLLM: what
     PagedAttention turned into", "The problem PagedAttention was actually solving").
   * The null block: the first block of the free queue is taken at construction and never
@@ -30,13 +31,13 @@ What it models (the pages on vLLM's paged KV cache):
     cost over all layers ("vLLM: what PagedAttention turned into", "Checking the 96.3%").
 
 Readings where the pages are silent (the C++ manager follows the same ones):
-  * Hash input: parent hash (32 bytes) || the block's 16 token ids as int32 little-endian ||
+  * Hash input: parent hash (32 bytes) || the block's token ids as int32 little-endian ||
     extra key bytes (the salt, first block only); the seed hash is SHA-256 of the seed string;
     the key is hash || group id (4 bytes, big-endian), group 0.
   * Within one free call the blocks are processed in the given order: each unhashed block is
     pushed to the front (so the last one pushed is reused first), each hashed block appended
     to the back.
-  * A prompt never hits in full: at most (len - 1) // 16 blocks come from the cache, so at
+  * A prompt never hits in full: at most (len - 1) // size blocks come from the cache, so at
     least one token is computed.
   * A full block is hashed and entered into the cache when the caller commits that its K/V has
     been computed; a hash already in the cache keeps its existing block and the new block
@@ -62,7 +63,7 @@ def none_hash(seed: str) -> bytes:
 
 
 def block_hash(parent: bytes, tokens: List[int], extra: bytes) -> bytes:
-    assert len(tokens) == BLOCK
+    """Hash of one full block: its tokens are all of the block (len(tokens) = block size)."""
     body = b"".join(int(t).to_bytes(4, "little", signed=True) for t in tokens)
     return sha256(parent + body + extra)
 
@@ -88,8 +89,10 @@ class Request:
 
 
 class BlockPool:
-    def __init__(self, num_blocks: int, enable_caching: bool = True, seed: str = "paged-kv-none-hash"):
-        assert num_blocks >= 2
+    def __init__(self, num_blocks: int, enable_caching: bool = True, seed: str = "paged-kv-none-hash",
+                 block_size: int = BLOCK):
+        assert num_blocks >= 2 and block_size > 0
+        self.bs = block_size
         self.blocks = [Block(i) for i in range(num_blocks)]
         self.queue: List[int] = list(range(num_blocks))  # front = index 0
         self.null = self.queue.pop(0)
@@ -145,40 +148,42 @@ class BlockPool:
         parent = hs[-1] if hs else self.root
         for k in range(len(hs), upto_blocks):
             extra = salt if k == 0 else b""
-            parent = block_hash(parent, tokens[k * BLOCK:(k + 1) * BLOCK], extra)
+            parent = block_hash(parent, tokens[k * self.bs:(k + 1) * self.bs], extra)
             hs.append(parent)
         return hs
 
     def add_request(self, rid: int, tokens: List[int], salt: bytes = b"") -> int:
         assert rid not in self.reqs and len(tokens) > 0
-        n_full = len(tokens) // BLOCK
+        bs = self.bs
+        n_full = len(tokens) // bs
         hs = self._hashes(tokens, salt, n_full, [])
         hits: List[int] = []
         if self.caching:
-            for k in range(min(n_full, (len(tokens) - 1) // BLOCK)):
+            for k in range(min(n_full, (len(tokens) - 1) // bs)):
                 lst = self.cache.get(hash_key(hs[k]))
                 if not lst:
                     break
                 hits.append(lst[0])
-        need = -(-len(tokens) // BLOCK) - len(hits)
+        need = -(-len(tokens) // bs) - len(hits)
         if need > len(self.queue) - sum(1 for i in hits if self.blocks[i].ref == 0):
             raise MemoryError("out of blocks")
         self._touch(hits)
         new = self._take(need)
-        r = Request(list(tokens), hits + new, salt, computed=len(hits) * BLOCK, hashes=hs[:len(hits)])
+        r = Request(list(tokens), hits + new, salt, computed=len(hits) * bs, hashes=hs[:len(hits)])
         self.reqs[rid] = r
         return r.computed
 
     def append_tokens(self, rid: int, tokens: List[int]) -> None:
         r = self.reqs[rid]
         pos0 = len(r.tokens)
-        need = sum(1 for p in range(pos0, pos0 + len(tokens)) if p % BLOCK == 0)
-        cow = len(tokens) > 0 and pos0 % BLOCK != 0 and self.blocks[r.blocks[-1]].ref > 1
+        bs = self.bs
+        need = sum(1 for p in range(pos0, pos0 + len(tokens)) if p % bs == 0)
+        cow = len(tokens) > 0 and pos0 % bs != 0 and self.blocks[r.blocks[-1]].ref > 1
         if need + int(cow) > len(self.queue):
             raise MemoryError("out of blocks")  # nothing changed
         for t in tokens:
             pos = len(r.tokens)
-            if pos % BLOCK == 0:
+            if pos % bs == 0:
                 r.blocks += self._take(1)
             else:
                 last = self.blocks[r.blocks[-1]]
@@ -193,7 +198,7 @@ class BlockPool:
         r = self.reqs[rid]
         assert num_computed <= len(r.tokens)
         r.computed = max(r.computed, num_computed)
-        n_full = r.computed // BLOCK
+        n_full = r.computed // self.bs
         r.hashes = self._hashes(r.tokens, r.salt, n_full, r.hashes)
         if not self.caching:
             return
@@ -223,7 +228,8 @@ class BlockPool:
 
     def slot_mapping(self, rid: int, first: int, n: int) -> List[int]:
         r = self.reqs[rid]
-        return [r.blocks[p // BLOCK] * BLOCK + p % BLOCK for p in range(first, first + n)]
+        bs = self.bs
+        return [r.blocks[p // bs] * bs + p % bs for p in range(first, first + n)]
 
     def take_copies(self) -> List[Tuple[int, int]]:
         c, self.copies = self.copies, []
@@ -231,13 +237,13 @@ class BlockPool:
 
 
 def num_blocks_for_memory(free_bytes: int, utilization: float, num_layers: int, num_kv_heads: int,
-                          head_dim: int, elem_bytes: int) -> int:
-    per_block = num_layers * 2 * num_kv_heads * BLOCK * head_dim * elem_bytes
+                          head_dim: int, elem_bytes: int, block_size: int = BLOCK) -> int:
+    per_block = num_layers * 2 * num_kv_heads * block_size * head_dim * elem_bytes
     return int(int(free_bytes * utilization) // per_block)
 
 
 def copy_blocks(k_cache, v_cache, pairs) -> None:
-    """Copy each (src, dst) block of both pools, every kv head (numpy arrays [NB, H, 16, D])."""
+    """Copy each (src, dst) block of both pools, every kv head (numpy arrays [NB, H, BS, D])."""
     for s, d in pairs:
         k_cache[d] = k_cache[s]
         v_cache[d] = v_cache[s]

@@ -26,7 +26,8 @@ EXPORTED = ("pa_reshape_and_cache", "pa_decode_workspace_size", "pa_decode", "pa
             "pa_bm_commit", "pa_bm_fork", "pa_bm_free_request", "pa_bm_get_blocks", "pa_bm_slot_mapping",
             "pa_bm_take_copies", "pa_bm_free_queue", "pa_bm_block_info", "pa_bm_num_blocks_for_memory", "pa_sha256",
             "pa_copy_blocks", "pa_reshape_and_cache_bs", "pa_decode_bs", "pa_prefill_chunk_bs",
-            "pa_copy_blocks_bs", "pa_step", "pa_decode_append")
+            "pa_copy_blocks_bs", "pa_step", "pa_decode_append", "pa_bm_create_bs",
+            "pa_bm_num_blocks_for_memory_bs")
 #: block sizes the *_bs entry points accept
 BLOCK_SIZES = (16, 32, 64, 128)
 #: size of the library's fixed scratch used by pa_decode_noalloc
@@ -116,6 +117,8 @@ def load(build_if_needed: bool = True) -> ctypes.CDLL:
                                                            i32, i32, i32, f32, ctypes.c_int, vp]),
                     ("pa_copy_blocks_bs", ctypes.c_int, [vp, vp, vp, i32, i32, i32, i32, i32, ctypes.c_int, vp]),
                     ("pa_step", ctypes.c_int, [ctypes.POINTER(StepDesc), vp]),
+                    ("pa_bm_create_bs", ctypes.c_int, [i32, i32, i32, ctypes.c_char_p, ctypes.POINTER(vp)]),
+                    ("pa_bm_num_blocks_for_memory_bs", i64, [sz, ctypes.c_double, i32, i32, i32, i32, ctypes.c_int]),
                     ("pa_decode_append", ctypes.c_int, [vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32,
                                                         i32, i32, i32, f32, ctypes.c_int, vp, sz, vp])):
                 fn = getattr(lib, name)
@@ -365,10 +368,14 @@ def pa_sha256(data: bytes) -> bytes:
 
 
 def pa_bm_num_blocks_for_memory(free_bytes: int, utilization: float, num_layers: int, num_kv_heads: int,
-                                head_dim: int, dtype) -> int:
+                                head_dim: int, dtype, block_size: int = BLOCK_SIZE) -> int:
     import torch
     code = dtype if isinstance(dtype, int) else (PA_F32 if dtype == torch.float32 else PA_BF16)
-    return int(load().pa_bm_num_blocks_for_memory(free_bytes, utilization, num_layers, num_kv_heads, head_dim, code))
+    if block_size == BLOCK_SIZE:
+        return int(load().pa_bm_num_blocks_for_memory(free_bytes, utilization, num_layers, num_kv_heads, head_dim,
+                                                      code))
+    return int(load().pa_bm_num_blocks_for_memory_bs(free_bytes, utilization, num_layers, num_kv_heads, head_dim,
+                                                     int(block_size), code))
 
 
 def _i32(xs):
@@ -379,11 +386,16 @@ def _i32(xs):
 class BlockManager:
     """The library's host block manager (pa_bm_* in include/pa.h), one per KV pool."""
 
-    def __init__(self, num_blocks: int, enable_caching: bool = True, hash_seed: Optional[str] = None):
+    def __init__(self, num_blocks: int, enable_caching: bool = True, hash_seed: Optional[str] = None,
+                 block_size: int = BLOCK_SIZE):
         h = ctypes.c_void_p()
-        _check("pa_bm_create", load().pa_bm_create(num_blocks, 1 if enable_caching else 0,
-                                                   None if hash_seed is None else hash_seed.encode(),
-                                                   ctypes.byref(h)))
+        seed = None if hash_seed is None else hash_seed.encode()
+        if block_size == BLOCK_SIZE:
+            _check("pa_bm_create", load().pa_bm_create(num_blocks, 1 if enable_caching else 0, seed, ctypes.byref(h)))
+        else:
+            _check("pa_bm_create_bs", load().pa_bm_create_bs(num_blocks, int(block_size), 1 if enable_caching else 0,
+                                                             seed, ctypes.byref(h)))
+        self.block_size = int(block_size)
         self._h = h
         self._lib = load()
 

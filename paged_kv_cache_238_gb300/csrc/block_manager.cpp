@@ -1,5 +1,5 @@
-// Host-side block manager for the paged KV pool: which physical 16-token blocks a request
-// owns, which freed blocks still hold reusable prefixes, and the block table / slot mapping
+// Host-side block manager for the paged KV pool: which physical blocks (16 tokens by default;
+// 32, 64 or 128 through pa_bm_create_bs) a request owns, which freed blocks still hold reusable prefixes, and the block table / slot mapping
 // the kernels read.
 //
 // Model ("vLLM: what PagedAttention turned into", "The block pool, and the two tricks in it"
@@ -13,11 +13,11 @@
 //    tail first, so a prefix's tail is offered for eviction before its parents.
 //  * Freed blocks keep their hash and stay in the cache map; a block is evicted from the map
 //    only when it is taken from the queue for new content.
-//  * A block hash is SHA-256(parent hash || the block's 16 token ids as int32 little-endian ||
+//  * A block hash is SHA-256(parent hash || the block's token ids as int32 little-endian ||
 //    extra key bytes), chained from SHA-256(seed); a per-request salt enters the first block
 //    only; the cache key appends the group id (4 bytes, big-endian). Prefix lookup takes the
 //    longest run of cached full blocks and stops at the first miss; a prompt never hits in
-//    full (at most (len - 1) / 16 blocks come from the cache).
+//    full (at most (len - 1) / block_size blocks come from the cache).
 //  * Blocks are reference counted: a forked request shares every block, and appending into a
 //    shared, partly filled last block first moves the request to a private copy
 //    (copy-on-write); the (source, destination) pairs wait for pa_copy_blocks.
@@ -37,7 +37,8 @@
 namespace pa {
 namespace bm {
 
-constexpr int32_t kBlockTokens = 16;
+constexpr int32_t kDefaultBlockTokens = 16;
+inline bool block_size_valid(int32_t bs) { return bs == 16 || bs == 32 || bs == 64 || bs == 128; }
 
 // ------------------------------------------------------------------------------------------
 // SHA-256 (FIPS 180-4): 64-byte blocks, 64 rounds; the round constants are the first 32 bits
@@ -146,15 +147,16 @@ Key make_key(const Hash& h, uint32_t group) {
     return k;
 }
 
-Hash hash_block(const Hash& parent, const int32_t* tokens, const uint8_t* extra, size_t extra_len) {
+// Hash of one full block of n tokens (the block size).
+Hash hash_block(const Hash& parent, const int32_t* tokens, int32_t n, const uint8_t* extra, size_t extra_len) {
     Sha256 s;
     s.update(parent.data(), parent.size());
-    uint8_t le[4 * kBlockTokens];
-    for (int i = 0; i < kBlockTokens; ++i) {
+    for (int32_t i = 0; i < n; ++i) {
         const uint32_t t = static_cast<uint32_t>(tokens[i]);
-        for (int b = 0; b < 4; ++b) le[4 * i + b] = static_cast<uint8_t>(t >> (8 * b));
+        uint8_t le[4];
+        for (int b = 0; b < 4; ++b) le[b] = static_cast<uint8_t>(t >> (8 * b));
+        s.update(le, 4);
     }
-    s.update(le, sizeof(le));
     if (extra_len) s.update(extra, extra_len);
     return s.digest();
 }
@@ -176,8 +178,8 @@ struct Request {
 
 class Manager {
   public:
-    Manager(int32_t num_blocks, bool caching, const std::string& seed)
-        : nb_(num_blocks), caching_(caching), recs_(num_blocks + 2) {
+    Manager(int32_t num_blocks, int32_t block_size, bool caching, const std::string& seed)
+        : nb_(num_blocks), bs_(block_size), caching_(caching), recs_(num_blocks + 2) {
         head_ = nb_;
         tail_ = nb_ + 1;
         recs_[head_].next = tail_;
@@ -197,25 +199,25 @@ class Manager {
         Request r;
         r.tokens.assign(tokens, tokens + n);
         if (salt_len > 0) r.salt.assign(salt, salt + salt_len);
-        const int32_t n_full = n / kBlockTokens;
+        const int32_t n_full = n / bs_;
         extend_hashes(r, n_full);
         std::vector<int32_t> hits;
         if (caching_) {
-            const int32_t max_hits = (n - 1) / kBlockTokens;
+            const int32_t max_hits = (n - 1) / bs_;
             for (int32_t k = 0; k < max_hits && k < n_full; ++k) {
                 auto it = cache_.find(make_key(r.hashes[k], 0));
                 if (it == cache_.end() || it->second.empty()) break;
                 hits.push_back(it->second.front());
             }
         }
-        const int32_t need = (n + kBlockTokens - 1) / kBlockTokens - static_cast<int32_t>(hits.size());
+        const int32_t need = (n + bs_ - 1) / bs_ - static_cast<int32_t>(hits.size());
         int32_t queued_hits = 0;
         for (int32_t b : hits) queued_hits += recs_[b].ref == 0 ? 1 : 0;
         if (need > free_ - queued_hits) return PA_ERR_NO_SPACE;
         for (int32_t b : hits) touch(b);
         r.blocks = hits;
         for (int32_t k = 0; k < need; ++k) r.blocks.push_back(take());
-        r.computed = static_cast<int32_t>(hits.size()) * kBlockTokens;
+        r.computed = static_cast<int32_t>(hits.size()) * bs_;
         r.hashes.resize(hits.size());
         if (num_cached) *num_cached = r.computed;
         reqs_.emplace(id, std::move(r));
@@ -230,12 +232,12 @@ class Manager {
         // first token lands in a shared, partly filled last block
         const int32_t pos0 = static_cast<int32_t>(r.tokens.size());
         int32_t need = 0;
-        for (int32_t p = pos0; p < pos0 + n; ++p) need += (p % kBlockTokens == 0) ? 1 : 0;
-        const bool cow = n > 0 && pos0 % kBlockTokens != 0 && recs_[r.blocks.back()].ref > 1;
+        for (int32_t p = pos0; p < pos0 + n; ++p) need += (p % bs_ == 0) ? 1 : 0;
+        const bool cow = n > 0 && pos0 % bs_ != 0 && recs_[r.blocks.back()].ref > 1;
         if (need + (cow ? 1 : 0) > free_) return PA_ERR_NO_SPACE;
         for (int32_t i = 0; i < n; ++i) {
             const int32_t pos = pos0 + i;
-            if (pos % kBlockTokens == 0) {
+            if (pos % bs_ == 0) {
                 r.blocks.push_back(take());
             } else if (recs_[r.blocks.back()].ref > 1) {
                 const int32_t src = r.blocks.back();
@@ -255,7 +257,7 @@ class Manager {
         Request& r = it->second;
         if (num_computed < 0 || num_computed > static_cast<int32_t>(r.tokens.size())) return PA_ERR_INVALID_ARG;
         if (num_computed > r.computed) r.computed = num_computed;
-        const int32_t n_full = r.computed / kBlockTokens;
+        const int32_t n_full = r.computed / bs_;
         extend_hashes(r, n_full);
         if (!caching_) return PA_OK;
         for (int32_t k = 0; k < n_full; ++k) {
@@ -318,13 +320,14 @@ class Manager {
     }
     int32_t ref(int32_t b) const { return (b >= 0 && b < nb_) ? recs_[b].ref : -1; }
     int32_t num_blocks() const { return nb_; }
+    int32_t block_size() const { return bs_; }
 
   private:
     void extend_hashes(Request& r, int32_t n_full) {
         for (int32_t k = static_cast<int32_t>(r.hashes.size()); k < n_full; ++k) {
             const Hash& parent = k == 0 ? root_ : r.hashes[k - 1];
             const bool first = k == 0;
-            r.hashes.push_back(hash_block(parent, r.tokens.data() + k * kBlockTokens,
+            r.hashes.push_back(hash_block(parent, r.tokens.data() + static_cast<size_t>(k) * bs_, bs_,
                                           first && !r.salt.empty() ? r.salt.data() : nullptr,
                                           first ? r.salt.size() : 0));
         }
@@ -387,6 +390,7 @@ class Manager {
     }
 
     int32_t nb_;
+    int32_t bs_;  // tokens per block
     bool caching_;
     std::vector<BlockRec> recs_;
     int32_t head_ = 0, tail_ = 0, null_ = 0, free_ = 0;
@@ -403,20 +407,26 @@ using pa::bm::Manager;
 
 struct pa_block_manager {
     Manager m;
-    pa_block_manager(int32_t nb, bool caching, const std::string& seed) : m(nb, caching, seed) {}
+    pa_block_manager(int32_t nb, int32_t bs, bool caching, const std::string& seed) : m(nb, bs, caching, seed) {}
 };
 
 extern "C" {
 
-PA_API pa_status pa_bm_create(int32_t num_blocks, int32_t enable_caching, const char* hash_seed,
-                              pa_block_manager** out) {
+PA_API pa_status pa_bm_create_bs(int32_t num_blocks, int32_t block_size, int32_t enable_caching,
+                                 const char* hash_seed, pa_block_manager** out) {
     if (!out || num_blocks < 2) return PA_ERR_INVALID_ARG;
     *out = nullptr;
-    pa_block_manager* bm = new (std::nothrow)
-        pa_block_manager(num_blocks, enable_caching != 0, hash_seed ? std::string(hash_seed) : "paged-kv-none-hash");
+    if (!pa::bm::block_size_valid(block_size)) return block_size > 0 ? PA_ERR_UNSUPPORTED : PA_ERR_INVALID_ARG;
+    pa_block_manager* bm = new (std::nothrow) pa_block_manager(
+        num_blocks, block_size, enable_caching != 0, hash_seed ? std::string(hash_seed) : "paged-kv-none-hash");
     if (!bm) return PA_ERR_NO_SPACE;
     *out = bm;
     return PA_OK;
+}
+
+PA_API pa_status pa_bm_create(int32_t num_blocks, int32_t enable_caching, const char* hash_seed,
+                              pa_block_manager** out) {
+    return pa_bm_create_bs(num_blocks, pa::bm::kDefaultBlockTokens, enable_caching, hash_seed, out);
 }
 
 PA_API void pa_bm_destroy(pa_block_manager* bm) { delete bm; }
@@ -465,12 +475,12 @@ PA_API pa_status pa_bm_slot_mapping(const pa_block_manager* bm, int64_t req_id, 
     if (!bm || n < 0 || first_pos < 0 || (n > 0 && !slots)) return PA_ERR_INVALID_ARG;
     const auto* r = bm->m.request(req_id);
     if (!r) return PA_ERR_INVALID_ARG;
-    const int64_t cap = static_cast<int64_t>(r->blocks.size()) * pa::bm::kBlockTokens;
+    const int64_t bs = bm->m.block_size();
+    const int64_t cap = static_cast<int64_t>(r->blocks.size()) * bs;
     if (static_cast<int64_t>(first_pos) + n > cap) return PA_ERR_INVALID_ARG;
     for (int32_t i = 0; i < n; ++i) {
         const int32_t p = first_pos + i;
-        slots[i] = static_cast<int64_t>(r->blocks[p / pa::bm::kBlockTokens]) * pa::bm::kBlockTokens +
-                   p % pa::bm::kBlockTokens;
+        slots[i] = static_cast<int64_t>(r->blocks[p / bs]) * bs + p % bs;
     }
     return PA_OK;
 }
@@ -498,14 +508,22 @@ PA_API pa_status pa_bm_block_info(const pa_block_manager* bm, int32_t block_id, 
     return PA_OK;
 }
 
-PA_API int64_t pa_bm_num_blocks_for_memory(size_t free_bytes, double utilization, int32_t num_layers,
-                                           int32_t num_kv_heads, int32_t head_dim, pa_dtype dtype) {
+PA_API int64_t pa_bm_num_blocks_for_memory_bs(size_t free_bytes, double utilization, int32_t num_layers,
+                                              int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                              pa_dtype dtype) {
     if (num_layers <= 0 || num_kv_heads <= 0 || head_dim <= 0 || !(utilization > 0.0) || utilization > 1.0) return -1;
+    if (!pa::bm::block_size_valid(block_size)) return -1;
     const int64_t el = dtype == PA_F32 ? 4 : (dtype == PA_BF16 ? 2 : 0);
     if (el == 0) return -1;
-    const int64_t per_block = static_cast<int64_t>(num_layers) * 2 * num_kv_heads * pa::bm::kBlockTokens * head_dim * el;
+    const int64_t per_block = static_cast<int64_t>(num_layers) * 2 * num_kv_heads * block_size * head_dim * el;
     const int64_t usable = static_cast<int64_t>(static_cast<double>(free_bytes) * utilization);
     return usable / per_block;
+}
+
+PA_API int64_t pa_bm_num_blocks_for_memory(size_t free_bytes, double utilization, int32_t num_layers,
+                                           int32_t num_kv_heads, int32_t head_dim, pa_dtype dtype) {
+    return pa_bm_num_blocks_for_memory_bs(free_bytes, utilization, num_layers, num_kv_heads, head_dim,
+                                          pa::bm::kDefaultBlockTokens, dtype);
 }
 
 PA_API pa_status pa_sha256(const uint8_t* data, size_t n, uint8_t* out32) {

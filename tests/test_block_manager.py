@@ -34,18 +34,19 @@ def _state(ref: BP.BlockPool, bm: B.BlockManager):
         assert h == (None if b.key is None else b.key[:32]), b.id
 
 
-def _run(seed: int, num_blocks: int, caching: bool, steps: int):
+def _run(seed: int, num_blocks: int, caching: bool, steps: int, block_size: int = 16):
     rng = random.Random(seed)
-    ref = BP.BlockPool(num_blocks, enable_caching=caching, seed="s%d" % seed)
-    bm = B.BlockManager(num_blocks, enable_caching=caching, hash_seed="s%d" % seed)
-    prefixes = [[rng.randrange(50) for _ in range(rng.randrange(1, 70))] for _ in range(4)]
+    ref = BP.BlockPool(num_blocks, enable_caching=caching, seed="s%d" % seed, block_size=block_size)
+    bm = B.BlockManager(num_blocks, enable_caching=caching, hash_seed="s%d" % seed, block_size=block_size)
+    scale = block_size // 16  # prompts and appends grow with the block size
+    prefixes = [[rng.randrange(50) for _ in range(rng.randrange(1, 70 * scale))] for _ in range(4)]
     salts = [b"", b"", b"tenant-a", b"tenant-b"]
     next_id = 1
     for _ in range(steps):
         live = sorted(ref.reqs)
         op = rng.random()
         if op < 0.3 or not live:
-            prompt = list(rng.choice(prefixes)) + [rng.randrange(50) for _ in range(rng.randrange(0, 40))]
+            prompt = list(rng.choice(prefixes)) + [rng.randrange(50) for _ in range(rng.randrange(0, 40 * scale))]
             salt = rng.choice(salts)
             try:
                 want = ref.add_request(next_id, prompt, salt)
@@ -58,7 +59,7 @@ def _run(seed: int, num_blocks: int, caching: bool, steps: int):
             next_id += 1
         elif op < 0.55:
             rid = rng.choice(live)
-            toks = [rng.randrange(50) for _ in range(rng.randrange(1, 20))]
+            toks = [rng.randrange(50) for _ in range(rng.randrange(1, 20 * scale))]
             try:
                 ref.append_tokens(rid, toks)
             except MemoryError:
@@ -93,6 +94,48 @@ def test_block_manager_matches_reference_model(seed):
     _run(seed, num_blocks=24 if seed % 2 else 64, caching=seed != 5, steps=400)
 
 
+@pytest.mark.parametrize("block_size,seed", [(32, 10), (64, 11), (128, 12), (32, 13)])
+def test_block_manager_matches_reference_model_larger_blocks(block_size, seed):
+    _run(seed, num_blocks=24 if seed % 2 else 48, caching=seed != 13, steps=300, block_size=block_size)
+
+
+def test_block_size_is_checked():
+    with pytest.raises(B.PaError) as e:
+        B.BlockManager(8, block_size=48)
+    assert e.value.status == B.PA_ERR_UNSUPPORTED
+    bm = B.BlockManager(8, block_size=64)
+    assert bm.add_request(1, list(range(65))) == 0
+    assert bm.block_ids(1) == [1, 2]
+    assert bm.slot_mapping(1, 63, 2) == [1 * 64 + 63, 2 * 64]
+
+
+def test_sha256_round_constants_are_the_cube_roots_of_the_first_primes():
+    """FIPS 180-4: the 64 round constants are the first 32 bits of the fractional parts of
+    the cube roots of the first 64 primes; the initial hash values likewise from the square
+    roots of the first 8. Derived here with exact integer roots and compared with the table in
+    the C++ source."""
+    import re
+    src = open(os.path.join(ROOT, "paged_kv_cache_238_gb300", "csrc", "block_manager.cpp")).read()
+    table = [int(x, 16) for x in re.findall(r"0x([0-9a-f]{8})u", src)]
+    primes = [p for p in range(2, 400) if all(p % d for d in range(2, int(p ** 0.5) + 1))]
+
+    def frac_bits(p, k):  # floor(frac(p^(1/k)) * 2^32) via the integer k-th root of p * 2^(32k)
+        x = p << (32 * k)
+        r = int(round(x ** (1.0 / k)))
+        while r ** k > x:
+            r -= 1
+        while (r + 1) ** k <= x:
+            r += 1
+        return r & 0xFFFFFFFF
+
+    cube = [frac_bits(p, 3) for p in primes[:64]]
+    square = [frac_bits(p, 2) for p in primes[:8]]
+    i = table.index(cube[0])
+    assert table[i:i + 64] == cube
+    j = table.index(square[0])
+    assert table[j:j + 8] == square
+
+
 def test_bad_calls_change_nothing():
     bm = B.BlockManager(8)
     bm.add_request(1, list(range(20)))
@@ -112,4 +155,7 @@ def test_pool_sizing_matches_reference():
     for args in [(80 * 2**30, 0.92, 32, 8, 128), (2**30, 0.5, 1, 4, 64)]:
         assert B.pa_bm_num_blocks_for_memory(*args, B.PA_BF16) == BP.num_blocks_for_memory(*args, 2)
         assert B.pa_bm_num_blocks_for_memory(*args, B.PA_F32) == BP.num_blocks_for_memory(*args, 4)
+        for bs in (32, 128):
+            assert (B.pa_bm_num_blocks_for_memory(*args, B.PA_BF16, block_size=bs) ==
+                    BP.num_blocks_for_memory(*args, 2, block_size=bs))
     assert B.pa_bm_num_blocks_for_memory(1 << 30, 1.5, 1, 1, 64, B.PA_BF16) == -1

@@ -19,8 +19,8 @@ from helpers import assert_close, to_dev, to_f64, to_host_bits  # noqa: E402
 pytestmark = pytest.mark.gpu
 
 
-def _pool(rng, nb, H, D, dtype):
-    shape = (nb, H, 16, D)
+def _pool(rng, nb, H, D, dtype, bs=16):
+    shape = (nb, H, bs, D)
     x = rng.standard_normal(shape).astype(np.float32)
     y = rng.standard_normal(shape).astype(np.float32)
     if dtype == "bf16":
@@ -54,13 +54,13 @@ def test_copy_blocks_out_of_range_pair_is_skipped_and_flagged():
     assert B.pa_get_device_errors(clear=True) == B.PA_DEVERR_BLOCK_RANGE
 
 
-@pytest.mark.parametrize("prompt_len", [37, 48])
-def test_fork_copy_on_write_decode_matches_oracle(prompt_len):
+@pytest.mark.parametrize("prompt_len,bs", [(37, 16), (48, 16), (100, 64), (128, 64), (70, 32)])
+def test_fork_copy_on_write_decode_matches_oracle(prompt_len, bs):
     rng = np.random.default_rng(100 + prompt_len)
     NB, Hq, Hkv, D = 32, 8, 2, 128
     scale = 1.0 / np.sqrt(D)
-    k_pool, v_pool = _pool(rng, NB, Hkv, D, "bf16")  # unowned cells hold arbitrary values
-    bm = B.BlockManager(NB)
+    k_pool, v_pool = _pool(rng, NB, Hkv, D, "bf16", bs)  # unowned cells hold arbitrary values
+    bm = B.BlockManager(NB, block_size=bs)
     kd, vd = to_dev(k_pool), to_dev(v_pool)
 
     def new_kv(n):
@@ -80,7 +80,7 @@ def test_fork_copy_on_write_decode_matches_oracle(prompt_len):
     for rid, tok in ((1, 1000), (2, 2000)):  # one sampled token per branch
         bm.append_tokens(rid, [tok])
     copies = bm.take_copies()
-    if prompt_len % 16:
+    if prompt_len % bs:
         assert len(copies) == 1  # the shared partial block was copied for the second branch
     if copies:
         pairs = np.array(copies, dtype=np.int32)

@@ -151,3 +151,26 @@ def test_copy_blocks_copies_both_pools():
     BP.copy_blocks(k, v, [(1, 4), (2, 5)])
     assert np.array_equal(k[4], k0[1]) and np.array_equal(v[5], v0[2])
     assert np.array_equal(k[:4], k0[:4])
+
+
+def test_larger_blocks_hash_all_their_tokens_and_cap_hits_by_block():
+    # "vLLM: what PagedAttention turned into": blocks of 16 to 128 tokens; a block hash covers
+    # the whole block, slots are block * size + offset, and a prompt never hits in full
+    bs = 32
+    p = BP.BlockPool(12, block_size=bs)
+    prompt = toks(2 * bs)
+    p.add_request(1, prompt)
+    assert p.block_ids(1) == [1, 2]
+    assert p.slot_mapping(1, bs - 1, 2) == [1 * bs + bs - 1, 2 * bs]
+    p.commit(1, len(prompt))
+    r = BP.none_hash("paged-kv-none-hash")
+    want = hashlib.sha256(r + np.array(prompt[:bs], dtype="<i4").tobytes()).digest()
+    assert p.reqs[1].hashes[0] == want
+    assert p.add_request(2, prompt) == bs            # (2 bs - 1) // bs = 1 block from the cache
+    assert p.add_request(3, toks(2 * bs + 1)) == 2 * bs
+
+
+def test_pool_sizing_scales_with_block_size():
+    n16 = BP.num_blocks_for_memory(2**34, 0.9, 4, 8, 128, 2)
+    n64 = BP.num_blocks_for_memory(2**34, 0.9, 4, 8, 128, 2, block_size=64)
+    assert n64 == int(int(2**34 * 0.9) // (4 * 2 * 8 * 64 * 128 * 2)) and n16 // 4 - 1 <= n64 <= n16 // 4
