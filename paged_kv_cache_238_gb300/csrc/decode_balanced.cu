@@ -261,7 +261,9 @@ __device__ __forceinline__ int32_t count_piece(int32_t* counter) {
     return old;
 }
 
-template <int D, int NW, int NH>  // NH: groups of 8 q heads (G <= 8 * NH)
+// NH: groups of 8 q heads (G <= 8 * NH). APPEND: the call appends each sequence's new token
+// (a separate instantiation, so plain decode carries none of its code).
+template <int D, int NW, int NH, bool APPEND>
 __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
     __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ block_table,
@@ -343,7 +345,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
     // attends over the page holding that position receives the token's K/V rows with the page,
     // uses them for that row and writes them to slot_mapping[i]: no kernel waits on its own pool
     // writes, and the writes cost no load latency on the streaming path.
-    const bool append = k_new != nullptr;
+    constexpr bool append = APPEND;
     constexpr int32_t CPR = D * 2 / 16;  // 16-byte chunks per K or V row
     const int32_t bs_log2 = sub_log2 + 4;
     // sequences without keys get zero rows (spread over the CTAs); with append their new rows
@@ -828,7 +830,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
     }
 }
 
-template <int D, int NW, int NH>
+template <int D, int NW, int NH, bool APPEND>
 cudaError_t launch_impl(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream) {
     alignas(64) CUtensorMap tm_k, tm_v;
     // Pool rows of head_dim elements: (block, kv head, token in block).
@@ -847,7 +849,7 @@ cudaError_t launch_impl(const DecodeArgs& a, const DecodePlan& plan, cudaStream_
     }
     if (e != cudaSuccess) return e;
     const int32_t G = a.num_q_heads / a.num_kv_heads;
-    e = cudaFuncSetAttribute(decode_balanced_kernel<D, NW, NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(decode_balanced_kernel<D, NW, NH, APPEND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(plan.smem_bytes));
     if (e != cudaSuccess) return e;
     BalWorkspace ws = bal_ws(a.workspace, a.num_seqs, a.num_kv_heads, G, D, plan.num_ctas);
@@ -864,7 +866,7 @@ cudaError_t launch_impl(const DecodeArgs& a, const DecodePlan& plan, cudaStream_
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_balanced_kernel<D, NW, NH>, tm_k, tm_v, static_cast<__nv_bfloat16*>(a.out),
+    return cudaLaunchKernelEx(&cfg, decode_balanced_kernel<D, NW, NH, APPEND>, tm_k, tm_v, static_cast<__nv_bfloat16*>(a.out),
                               static_cast<const __nv_bfloat16*>(a.q), a.block_table, a.max_blocks_per_seq,
                               a.seq_lens, a.num_seqs, a.num_kv_heads, G, a.num_blocks,
                               block_size_log2(a.block_size) - 4, a.scale * kLog2e, plan.stages, plan.stage_bytes, ws,
@@ -876,10 +878,10 @@ cudaError_t launch_impl(const DecodeArgs& a, const DecodePlan& plan, cudaStream_
 template <int D, int NW>
 int ctas_per_sm(uint32_t smem) {
     int n = 0;
-    if (cudaFuncSetAttribute(decode_balanced_kernel<D, NW, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(decode_balanced_kernel<D, NW, 2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
         return 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_balanced_kernel<D, NW, 2>, NW * 32, smem) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_balanced_kernel<D, NW, 2, true>, NW * 32, smem) !=
         cudaSuccess)
         return 0;
     return n;
@@ -913,14 +915,23 @@ bool plan_decode_balanced(int32_t S, int32_t Hkv, int32_t G, int32_t D, const De
     return false;
 }
 
+namespace {
+template <int D, int NW>
+cudaError_t pick(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream, bool wide) {
+    if (a.k_new != nullptr)
+        return wide ? launch_impl<D, NW, 2, true>(a, plan, stream) : launch_impl<D, NW, 1, true>(a, plan, stream);
+    return wide ? launch_impl<D, NW, 2, false>(a, plan, stream) : launch_impl<D, NW, 1, false>(a, plan, stream);
+}
+}  // namespace
+
 cudaError_t launch_decode_balanced(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream) {
     const bool wide = a.num_q_heads / a.num_kv_heads > 8;  // 9..16 q heads per kv head
     if (a.head_dim == 128) {
-        if (plan.warps == 8) return wide ? launch_impl<128, 8, 2>(a, plan, stream) : launch_impl<128, 8, 1>(a, plan, stream);
-        return wide ? launch_impl<128, 4, 2>(a, plan, stream) : launch_impl<128, 4, 1>(a, plan, stream);
+        if (plan.warps == 8) return pick<128, 8>(a, plan, stream, wide);
+        return pick<128, 4>(a, plan, stream, wide);
     }
-    if (plan.warps == 8) return wide ? launch_impl<64, 8, 2>(a, plan, stream) : launch_impl<64, 8, 1>(a, plan, stream);
-    return wide ? launch_impl<64, 4, 2>(a, plan, stream) : launch_impl<64, 4, 1>(a, plan, stream);
+    if (plan.warps == 8) return pick<64, 8>(a, plan, stream, wide);
+    return pick<64, 4>(a, plan, stream, wide);
 }
 
 }  // namespace pa

@@ -147,3 +147,30 @@ def test_step_in_a_cuda_graph_and_timing_events():
     assert np.array_equal(to_host_bits(dw.out_prefill), eager_pre)
     assert np.array_equal(to_host_bits(dw.out), eager_dec)  # same split, same bits
     _check(dw, what="graph replay")
+
+
+@pytest.mark.slow
+def test_full_mixed_step_through_pa_step_sampled_rows():
+    """The mixed-step workload at full size, in the launch configuration the benchmark times
+    (pa_step, decode on half the SMs): sampled decode rows and prefill rows against the oracle
+    and the pool bit-exact."""
+    wl = W.mixed_step()
+    dw = DeviceWorkload(wl)
+    _step(dw)
+    torch.cuda.synchronize()
+    kc, vc = dw.host_pool_after_writes()
+    assert np.array_equal(to_host_bits(dw.k_cache)[1:], kc[1:])
+    rng = np.random.default_rng(9)
+    rows = np.sort(rng.choice(wl.S, size=40, replace=False))
+    ref = oracle.attention(wl.q[rows], kc, vc, wl.block_table[rows], wl.seq_lens[rows], wl.scale)
+    assert_close(to_f64(dw.out)[rows], ref, "bf16", "pa_step decode rows")
+    qsl = wl.query_start_loc
+    picks = []
+    for i in range(len(qsl) - 1):
+        C, L = int(qsl[i + 1] - qsl[i]), int(wl.seq_lens_prefill[i])
+        for r in sorted(set(rng.choice(C, size=4, replace=False).tolist()) | {0, C - 1}):
+            picks.append((int(qsl[i]) + r, i, L - C + r + 1))
+    prow = np.array([p[0] for p in picks])
+    ref = oracle.attention(wl.q_prefill[prow], kc, vc, wl.block_table_prefill[[p[1] for p in picks]],
+                           np.array([p[2] for p in picks], np.int32), wl.scale)
+    assert_close(to_f64(dw.out_prefill)[prow], ref, "bf16", "pa_step prefill rows")
