@@ -251,6 +251,23 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest value over the job's ranks: a job's time is that of its slowest rank."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: float, world: int, seconds: float) -> float:
+    """Whole-job throughput under weak scaling: every rank processes its own units (replicas,
+    no exchange), so the job's units are world x the per-rank units over the slowest time."""
+    return units_per_rank * world / seconds
+
+
 def to_dev(a, dev):
     import torch
     if a.dtype == np.uint16:
@@ -589,12 +606,7 @@ def run_ours(args):
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
-        ms = t0.elapsed_time(t1)
-        if world > 1:
-            tt = torch.tensor([ms], device=dev, dtype=torch.float64)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            ms = float(tt.item())
-        return ms
+        return max_over_ranks(t0.elapsed_time(t1), world, dev)
 
     sampler = ClockSampler(local)
     sampler.start()
@@ -637,16 +649,16 @@ def run_ours(args):
     tokens = (wl.S if step.has_dec else 0) + (int(wl.query_start_loc[-1]) if step.has_pre else 0)
     if args.workload == "mixed_step":
         metric, unit, nd = MIXED_METRIC, "tokens/s", 1
-        value = tokens * world / (ms_step * 1e-3)
-        e2e_value = tokens * world / (ms_e2e / K * 1e-3)
+        value = job_rate(tokens, world, ms_step * 1e-3)
+        e2e_value = job_rate(tokens, world, ms_e2e / K * 1e-3)
     elif args.workload == "prefill_chunks":
         metric, unit, nd = PREFILL_METRIC, "TFLOP/s", 2
-        value = nbytes["prefill_flops"] * world / (ms_step * 1e-3) / 1e12
-        e2e_value = nbytes["prefill_flops"] * world / (ms_e2e / K * 1e-3) / 1e12
+        value = job_rate(nbytes["prefill_flops"], world, ms_step * 1e-3) / 1e12
+        e2e_value = job_rate(nbytes["prefill_flops"], world, ms_e2e / K * 1e-3) / 1e12
     else:
         metric, unit, nd = METRIC, "TB/s", 4
-        value = nbytes["step"] * world / (ms_step * 1e-3) / 1e12
-        e2e_value = nbytes["step"] * world / (ms_e2e / K * 1e-3) / 1e12
+        value = job_rate(nbytes["step"], world, ms_step * 1e-3) / 1e12
+        e2e_value = job_rate(nbytes["step"], world, ms_e2e / K * 1e-3) / 1e12
     line = {
         "metric": metric, "value": round(value, nd), "unit": unit, "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_step, 6), "higher_is_better": True,
