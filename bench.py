@@ -422,6 +422,10 @@ class DeviceStep:
         self.out_arena = self._pack(out_names, dev, copy=False)
         self.inputs = [getattr(self, n) for n in in_names]
         self.outputs = [getattr(self, n) for n in out_names]
+        # buffer sets: 0 = the tensors above; add_buffer() makes more with the same layout
+        self.in_names, self.out_names = in_names, out_names
+        self.bufs = [{n: getattr(self, n) for n in in_names + out_names}]
+        self.in_arenas, self.out_arenas = [self.in_arena], [self.out_arena]
         # whole step through pa_step: prefill and decode side by side on an SM split
         self.whole_step = whole_step and self.has_pre and self.has_dec
         # decode-only step with one new token per sequence: pa_decode_append (write + attention)
@@ -449,9 +453,27 @@ class DeviceStep:
             setattr(self, n, v)
         return arena
 
-    def __call__(self, i: int, ev=None):
-        """Step i on pool i % R; ev maps a kernel name to an event pair recorded around it."""
+    def add_buffer(self) -> int:
+        """Another set of input and output buffers (same layout); returns its index."""
+        import torch
+        ia, oa = torch.empty_like(self.in_arena), torch.empty_like(self.out_arena)
+        ia.copy_(self.in_arena)
+        views = {}
+        for names, old, new in ((self.in_names, self.in_arena, ia), (self.out_names, self.out_arena, oa)):
+            for n in names:
+                t = self.bufs[0][n]
+                off = t.data_ptr() - old.data_ptr()
+                views[n] = new[off:off + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+        self.bufs.append(views)
+        self.in_arenas.append(ia)
+        self.out_arenas.append(oa)
+        return len(self.bufs) - 1
+
+    def __call__(self, i: int, ev=None, buf: int = 0):
+        """Step i on pool i % R with buffer set `buf`; ev maps a kernel name to an event pair
+        recorded around it."""
         B, r, s, wl = self.B, i % self.R, self.stream, self.wl
+        T = self.bufs[buf]
 
         def rec(k, j):
             if ev is not None and k in ev:
@@ -462,32 +484,32 @@ class DeviceStep:
             if ev is not None:
                 tev = [ev[k][j] if k in ev else None for k in ("reshape", "prefill", "decode") for j in (0, 1)]
             B.pa_step(self.kcs[r], self.vcs[r], wl.scale,
-                      k_new=self.k_new if self.has_new else None, v_new=self.v_new if self.has_new else None,
-                      slot_mapping=self.slots if self.has_new else None,
-                      prefill_out=self.outp, prefill_q=self.qp, prefill_block_table=self.btp, prefill_seq_lens=self.lp,
-                      query_start_loc=self.qsl, max_chunk_len=self.max_chunk, prefill_max_seq_len=self.msl_p,
-                      decode_out=self.out, decode_q=self.q, decode_block_table=self.bt, decode_seq_lens=self.lens,
+                      k_new=T["k_new"] if self.has_new else None, v_new=T["v_new"] if self.has_new else None,
+                      slot_mapping=T["slots"] if self.has_new else None,
+                      prefill_out=T["outp"], prefill_q=T["qp"], prefill_block_table=T["btp"], prefill_seq_lens=T["lp"],
+                      query_start_loc=T["qsl"], max_chunk_len=self.max_chunk, prefill_max_seq_len=self.msl_p,
+                      decode_out=T["out"], decode_q=T["q"], decode_block_table=T["bt"], decode_seq_lens=T["lens"],
                       decode_max_seq_len=self.msl, workspace=self.ws, decode_sms=self.decode_sms,
                       timing_events=tev, stream=s)
             return
         if self.fused_append:
             rec("decode", 0)
-            B.pa_decode_append(self.out, self.q, self.k_new, self.v_new, self.slots, self.kcs[r], self.vcs[r], self.bt,
-                               self.lens, self.msl, wl.scale, self.ws, stream=s)
+            B.pa_decode_append(T["out"], T["q"], T["k_new"], T["v_new"], T["slots"], self.kcs[r], self.vcs[r], T["bt"],
+                               T["lens"], self.msl, wl.scale, self.ws, stream=s)
             rec("decode", 1)
             return
         if self.has_new:
             rec("reshape", 0)
-            B.pa_reshape_and_cache(self.k_new, self.v_new, self.kcs[r], self.vcs[r], self.slots, stream=s)
+            B.pa_reshape_and_cache(T["k_new"], T["v_new"], self.kcs[r], self.vcs[r], T["slots"], stream=s)
             rec("reshape", 1)
         if self.has_pre:
             rec("prefill", 0)
-            B.pa_prefill_chunk(self.outp, self.qp, self.kcs[r], self.vcs[r], self.btp, self.lp, self.qsl,
+            B.pa_prefill_chunk(T["outp"], T["qp"], self.kcs[r], self.vcs[r], T["btp"], T["lp"], T["qsl"],
                                self.max_chunk, self.msl_p, wl.scale, stream=s)
             rec("prefill", 1)
         if self.has_dec:
             rec("decode", 0)
-            B.pa_decode(self.out, self.q, self.kcs[r], self.vcs[r], self.bt, self.lens, self.msl, wl.scale,
+            B.pa_decode(T["out"], T["q"], self.kcs[r], self.vcs[r], T["bt"], T["lens"], self.msl, wl.scale,
                         self.ws, stream=s)
             rec("decode", 1)
 
@@ -576,20 +598,59 @@ def run_ours(args):
     n_main = K // chunk
 
     # ---- e2e graph: pinned host inputs in, results out, every step ------------------------
-    # the step's inputs and outputs are packed in one device buffer each (DeviceStep), so a
-    # step moves them with one copy each way
+    # The step's inputs and outputs are packed in one device buffer each (DeviceStep), so a
+    # step moves them with one copy each way. Two buffer sets alternate: step i+1's inputs
+    # travel host -> device on one copy stream while step i computes, and step i's outputs
+    # travel back on another once it is done (the two directions use separate copy engines);
+    # every step's copies are inside the timed region.
+    step.add_buffer()
     h_in = step.in_arena.cpu().pin_memory()
     h_out = torch.empty(step.out_arena.shape, dtype=torch.uint8, pin_memory=True)
     h2d = h_in.numel()
     d2h = h_out.numel()
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
 
-    def e2e_step(i):
-        step.in_arena.copy_(h_in, non_blocking=True)
-        step(i)
-        h_out.copy_(step.out_arena, non_blocking=True)
+    def e2e_chunk(n):
+        ev = torch.cuda.Event
+        start = ev()
+        start.record(stream)
+        s_in.wait_event(start)
+        s_out.wait_event(start)
+        copied, done, sent = [ev() for _ in range(n)], [ev() for _ in range(n)], [ev() for _ in range(n)]
+        with torch.cuda.stream(s_in):
+            step.in_arenas[0].copy_(h_in, non_blocking=True)
+            copied[0].record(s_in)
+        for i in range(n):
+            b = i % 2
+            stream.wait_event(copied[i])      # step i's inputs landed
+            if i >= 2:
+                stream.wait_event(sent[i - 2])  # step i-2's outputs (same buffer set) have left
+            step(i, buf=b)
+            done[i].record(stream)
+            if i + 1 < n:
+                with torch.cuda.stream(s_in):
+                    if i >= 1:
+                        s_in.wait_event(done[i - 1])  # buffer set (i + 1) % 2 is free again
+                    step.in_arenas[(i + 1) % 2].copy_(h_in, non_blocking=True)
+                    copied[i + 1].record(s_in)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(done[i])
+                h_out.copy_(step.out_arenas[b], non_blocking=True)
+                sent[i].record(s_out)
+        for s_ in (s_in, s_out):
+            end = ev()
+            end.record(s_)
+            stream.wait_event(end)
 
-    g_e2e = capture(e2e_step, chunk, False)
-    g_e2e_rem = capture(e2e_step, rem, False) if rem else None
+    def capture_e2e(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+                e2e_chunk(n)
+        return g
+
+    g_e2e = capture_e2e(chunk)
+    g_e2e_rem = capture_e2e(rem) if rem else None
 
     def timed(gm, gr):
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
