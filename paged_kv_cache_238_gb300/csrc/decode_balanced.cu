@@ -296,6 +296,10 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
 
     // Inputs may come from the kernel before this one in the stream (programmatic launch).
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Let the next kernel's grid be launched now: its CTAs take an SM as soon as one of ours
+    // leaves it (a second decode CTA does not fit beside this one) and wait there for this grid
+    // to complete, so the launch latency hides behind our merge tail.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // ---- prologue: clamped lengths and units per sequence, block-wide exclusive scan -------
     {
