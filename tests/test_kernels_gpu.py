@@ -305,3 +305,36 @@ def test_mixed_step_prefill_rows_sampled():
     assert_close(out[rows], ref, "bf16", "mixed step, prefill rows")
     # the pool after the step's writes is bit-exact too
     check_pool(dw, kc, vc)
+
+
+# ----------------------------------------------------------------------------- maximum sizes
+
+@pytest.mark.parametrize("S", [1024, 1025])
+def test_decode_at_and_past_the_persistent_path_batch_limit(S):
+    """1024 sequences is the largest batch whose tables the persistent kernel keeps in shared
+    memory; 1025 takes the general path. Both against the oracle."""
+    rng = np.random.default_rng(700 + S)
+    lens = rng.integers(1, 40, size=S)
+    wl = W.build_decode(700 + S, lens, H_q=8, H_kv=2, D=64, num_blocks=int(np.sum(-(-lens // 16))) + 2,
+                        dtype="bf16")
+    _decode_vs_oracle(wl, what=f"{S} sequences")
+
+
+def test_decode_block_ids_at_the_top_of_a_large_pool():
+    """A pool of 200 000 blocks whose tables name the highest ids (pool rows far past 2^24)."""
+    NB, H_kv, D = 200_000, 1, 64
+    lens = np.array([33, 700, 16, 1])
+    wl = W.build_decode(710, lens, H_q=4, H_kv=H_kv, D=D, num_blocks=64, dtype="bf16", new_token=False,
+                        poison=False)
+    # move every used block to the top of a large pool
+    used = sorted(set(wl.block_table[wl.block_table > 0].tolist()))
+    remap = {b: NB - 1 - i for i, b in enumerate(used)}
+    kc = np.zeros((NB, H_kv, 16, D), np.uint16)
+    vc = np.zeros_like(kc)
+    for b, nb in remap.items():
+        kc[nb], vc[nb] = wl.k_cache[b], wl.v_cache[b]
+    bt = np.vectorize(lambda x: remap.get(int(x), 0))(wl.block_table).astype(np.int32)
+    wl2 = W.Workload(name="top", dtype="bf16", H_q=4, H_kv=H_kv, D=D, num_blocks=NB, scale=wl.scale, k_cache=kc,
+                     v_cache=vc, q=wl.q, block_table=bt, seq_lens=wl.seq_lens)
+    assert bt.max() == NB - 1
+    _decode_vs_oracle(wl2, what="top of a large pool")
