@@ -761,7 +761,7 @@ def run_ours(args):
         line["roofline"]["kernel"] = KERNEL_LABEL["decode_append"]
     if step.whole_step:
         line["config"]["step_call"] = (f"pa_step: reshape_and_cache, then prefill and decode side by side "
-                                       f"(decode on {args.decode_sms or 'half the'} SMs)")
+                                       f"(decode on {args.decode_sms or '27/64 of the'} SMs)")
         line["config"]["kernel_timing"] += "; prefill and decode overlap, so their durations add up to more than the step"
     if args.workload == "gqa_decode":
         line["config"]["decode_bytes_per_call"] = nbytes["decode"]
@@ -847,7 +847,7 @@ def main(argv=None):
     ap.add_argument("--no-cupti", action="store_true", help="skip the activity-trace launch count (e.g. under ncu)")
     ap.add_argument("--sequential", action="store_true",
                     help="one call per kernel: no pa_step (mixed step) and no pa_decode_append (decode step)")
-    ap.add_argument("--decode-sms", type=int, default=0, help="pa_step: SMs held by decode (0 = half)")
+    ap.add_argument("--decode-sms", type=int, default=0, help="pa_step: SMs held by decode (0 = 27/64 of them)")
     args = ap.parse_args(argv)
     _, _, default_steps, default_replicas = WORKLOADS[args.workload]
     if args.steps is None:

@@ -281,8 +281,10 @@ PA_API pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache
  *
  * A part with zero sequences (or zero new tokens) is skipped and its pointers may be NULL.
  * Every argument is checked as the separate entry point would check it before anything is
- * launched. decode_sms: 0 = half of the device's SMs; otherwise 1..num_SMs (larger values are
- * clamped). workspace: >= pa_decode_workspace_size(num_decode_seqs, ...) bytes, as for
+ * launched. decode_sms: 0 = 27/64 of the device's SMs (64 of 152, the best split measured for
+ * a step of 2 GB of decode KV beside 16 x 512-token prefill chunks); otherwise 1..num_SMs
+ * (larger values are clamped). On a capped grid the decode kernel runs 10 warps per CTA.
+ * workspace: >= pa_decode_workspace_size(num_decode_seqs, ...) bytes, as for
  * pa_decode. timing_events: NULL, or six cudaEvent_t (each may be NULL) recorded before and
  * after reshape_and_cache, prefill and decode on the stream each kernel runs on, for the
  * caller's profiling; they are recorded as external events, so under stream capture they

@@ -276,7 +276,8 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
     constexpr int KS = D / 16;  // k-steps over head_dim
     constexpr int E = D / 32;   // elements per lane in the merges
     constexpr int NTH = NW * 32;
-    static_assert(NW <= 8, "level-2 reductions cover the pieces of at most 8 warps");
+    static_assert(NW <= 16, "level-2 reductions cover the pieces of at most 16 warps");
+    constexpr int kPieceLanes = NW > 8 ? 16 : 8;  // lanes that can hold a group's pieces
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const BalLayout L = bal_layout(NW, nst, stage_bytes, G, D, S);
@@ -757,7 +758,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
 #pragma unroll
             for (int k = 0; k < 4; ++k) Mk[k] = mk[k];
 #pragma unroll
-            for (int off = 4; off > 0; off >>= 1)  // a group has at most NW <= 8 pieces, in lanes 0..7
+            for (int off = kPieceLanes / 2; off > 0; off >>= 1)  // a group has at most NW pieces
 #pragma unroll
                 for (int k = 0; k < 4; ++k) Mk[k] = fmaxf(Mk[k], __shfl_xor_sync(0xffffffffu, Mk[k], off));
 #pragma unroll
@@ -766,7 +767,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
                 dk[k] = lk[k] * wk[k];
             }
 #pragma unroll
-            for (int off = 4; off > 0; off >>= 1)
+            for (int off = kPieceLanes / 2; off > 0; off >>= 1)
 #pragma unroll
                 for (int k = 0; k < 4; ++k) dk[k] += __shfl_xor_sync(0xffffffffu, dk[k], off);
 #pragma unroll
@@ -879,13 +880,17 @@ cudaError_t launch_impl(const DecodeArgs& a, const DecodePlan& plan, cudaStream_
                               static_cast<int4*>(const_cast<void*>(a.v_cache)));
 }
 
+// CTAs of the NW-warp kernel that fit on one SM with `smem` bytes of dynamic shared memory
+// (checked on the 2-group instantiation, the one with the most registers; 10-warp CTAs exist
+// without append only).
 template <int D, int NW>
 int ctas_per_sm(uint32_t smem) {
+    constexpr bool A = NW != 10;
     int n = 0;
-    if (cudaFuncSetAttribute(decode_balanced_kernel<D, NW, 2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(decode_balanced_kernel<D, NW, 2, A>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
         return 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_balanced_kernel<D, NW, 2, true>, NW * 32, smem) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_balanced_kernel<D, NW, 2, A>, NW * 32, smem) !=
         cudaSuccess)
         return 0;
     return n;
@@ -897,13 +902,25 @@ bool plan_decode_balanced(int32_t S, int32_t Hkv, int32_t G, int32_t D, const De
                           int32_t max_ctas, bool append) {
     if (G < 4 || G > kBalMaxGroup || (D != 64 && D != 128) || S > kBalMaxSeqs || S < 1) return false;
     const uint32_t stage = bal_stage_bytes(D, G, append);
-    // Prefer 8 streaming warps per CTA with as many stages as fit; 4 warps for large groups.
-    for (int NW : {8, 4}) {
+    // Prefer 8 streaming warps per CTA with as many stages as fit; 4 warps for large groups. A
+    // grid capped below the SM count (decode beside another kernel, no append) streams on few
+    // SMs, where each warp's page loop sets the rate: there 10 warps come first.
+    const bool capped = max_ctas > 0 && max_ctas < dev.num_sms && !append;
+    const int order_capped[] = {10, 8, 4}, order_full[] = {8, 4};
+    const int* order = capped ? order_capped : order_full;
+    const int n_order = capped ? 3 : 2;
+    for (int oi = 0; oi < n_order; ++oi) {
+        const int NW = order[oi];
         for (int nst = 4; nst >= 2; --nst) {
             const BalLayout L = bal_layout(NW, nst, stage, G, D, S);
             if (L.total > static_cast<uint32_t>(dev.max_smem_optin)) continue;
-            const int per_sm = (D == 128) ? (NW == 8 ? ctas_per_sm<128, 8>(L.total) : ctas_per_sm<128, 4>(L.total))
-                                          : (NW == 8 ? ctas_per_sm<64, 8>(L.total) : ctas_per_sm<64, 4>(L.total));
+            int per_sm = 0;
+            if (D == 128)
+                per_sm = NW == 10 ? ctas_per_sm<128, 10>(L.total)
+                                  : NW == 8 ? ctas_per_sm<128, 8>(L.total) : ctas_per_sm<128, 4>(L.total);
+            else
+                per_sm = NW == 10 ? ctas_per_sm<64, 10>(L.total)
+                                  : NW == 8 ? ctas_per_sm<64, 8>(L.total) : ctas_per_sm<64, 4>(L.total);
             if (per_sm < 1) continue;
             plan->path = kDecodeMmaBalanced;
             plan->warps = NW;
@@ -920,6 +937,13 @@ bool plan_decode_balanced(int32_t S, int32_t Hkv, int32_t G, int32_t D, const De
 }
 
 namespace {
+// 10-warp CTAs serve capped grids without append only (their plan never sets k_new).
+template <int D, int NW>
+cudaError_t pick_plain(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream, bool wide) {
+    if (a.k_new != nullptr) return cudaErrorInvalidValue;
+    return wide ? launch_impl<D, NW, 2, false>(a, plan, stream) : launch_impl<D, NW, 1, false>(a, plan, stream);
+}
+
 template <int D, int NW>
 cudaError_t pick(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream, bool wide) {
     if (a.k_new != nullptr)
@@ -931,9 +955,11 @@ cudaError_t pick(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t strea
 cudaError_t launch_decode_balanced(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream) {
     const bool wide = a.num_q_heads / a.num_kv_heads > 8;  // 9..16 q heads per kv head
     if (a.head_dim == 128) {
+        if (plan.warps == 10) return pick_plain<128, 10>(a, plan, stream, wide);
         if (plan.warps == 8) return pick<128, 8>(a, plan, stream, wide);
         return pick<128, 4>(a, plan, stream, wide);
     }
+    if (plan.warps == 10) return pick_plain<64, 10>(a, plan, stream, wide);
     if (plan.warps == 8) return pick<64, 8>(a, plan, stream, wide);
     return pick<64, 4>(a, plan, stream, wide);
 }

@@ -152,7 +152,7 @@ def test_step_in_a_cuda_graph_and_timing_events():
 @pytest.mark.slow
 def test_full_mixed_step_through_pa_step_sampled_rows():
     """The mixed-step workload at full size, in the launch configuration the benchmark times
-    (pa_step, decode on half the SMs): sampled decode rows and prefill rows against the oracle
+    (pa_step, its default SM split): sampled decode rows and prefill rows against the oracle
     and the pool bit-exact."""
     wl = W.mixed_step()
     dw = DeviceWorkload(wl)
