@@ -322,6 +322,7 @@ def pa_step(k_cache, v_cache, scale: float, k_new=None, v_new=None, slot_mapping
     """One whole mixed step (C ABI pa_step): reshape_and_cache of the new tokens, then chunked
     prefill and decode attention side by side. A part whose tensors are None is skipped.
     k_cache, v_cache: [NB, H_kv, BS, D]; the other tensors as for the single-kernel calls.
+    decode_sms: SMs held by the decode kernel while prefill runs (0 = 27/64 of them).
     timing_events: None or six torch.cuda.Event (or None) recorded before/after reshape,
     prefill and decode on the stream each kernel runs on."""
     _need_cuda(k_cache, v_cache, k_new, v_new, slot_mapping, prefill_out, prefill_q, prefill_block_table,
