@@ -437,7 +437,8 @@ PA_API pa_status pa_step(const pa_step_desc* d, void* stream_ptr) {
     DecodePlan plan{};
     if (has_dec) {
         const int32_t n = dev->info.num_sms;
-        const int32_t sms = d->decode_sms == 0 ? (n * 27) / 64 : (d->decode_sms < n ? d->decode_sms : n);
+        const int32_t dflt = (n * 27) / 64 > 0 ? (n * 27) / 64 : 1;  // 64 of 152 SMs
+        const int32_t sms = d->decode_sms == 0 ? dflt : (d->decode_sms < n ? d->decode_sms : n);
         st = plan_checked_decode(da, dev->info, has_pre ? sms : 0, &plan);
         if (st != PA_OK) return st;
     }
