@@ -46,6 +46,7 @@ constexpr int kMmaWarp = 1;         // tensor-memory owner and MMA issuer
 constexpr int kSoftWarp0 = 2;       // warps 2-5: softmax of Q tile a; warps 6-9: Q tile b
 constexpr int kVWarp = 10;          // V producer
 constexpr int kTcThreads = 32 * (kVWarp + 1);
+constexpr int kLptMaxSeqs = 64;  // sequences ordered longest first inside the kernel
 constexpr int kSoftmaxThreads = 256;  // both softmax warpgroups
 constexpr uint32_t kHalf = 16384;     // 128 rows x 128 bytes (64 bf16 columns)
 constexpr uint32_t kTile = 2 * kHalf; // a 128 x 128 bf16 operand
@@ -125,8 +126,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
 
     const int32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // Q tile pairs of one (sequence, kv head) are adjacent in launch order, so they run at the
-    // same time and read each K/V tile from L2 after the first of them brings it in.
-    const int32_t seq = blockIdx.z, h = blockIdx.y;
+    // same time and read each K/V tile from L2 after the first of them brings it in. Up to 64
+    // sequences go in order of decreasing total length (ties by index): CTA z takes the
+    // sequence of rank z, so the longest CTAs start first and the grid ends on short ones.
+    __shared__ int32_t lpt_len[kLptMaxSeqs];
+    __shared__ int32_t lpt_seq;
+    int32_t seq = blockIdx.z;
+    const int32_t n_seqs = static_cast<int32_t>(gridDim.z);
+    if (n_seqs <= kLptMaxSeqs) {
+        if (tid < n_seqs) lpt_len[tid] = __ldg(seq_lens + tid);
+        __syncthreads();
+        if (tid < n_seqs) {
+            const int32_t mine = lpt_len[tid];
+            int32_t rank = 0;
+            for (int32_t u = 0; u < n_seqs; ++u) {
+                const int32_t o = lpt_len[u];
+                rank += (o > mine || (o == mine && u < tid)) ? 1 : 0;
+            }
+            if (rank == static_cast<int32_t>(blockIdx.z)) lpt_seq = tid;
+        }
+        __syncthreads();
+        seq = lpt_seq;
+    }
+    const int32_t h = blockIdx.y;
     const int32_t pair = gridDim.x - 1 - blockIdx.x;  // the longest pairs start first
     const int32_t Hq = G * num_kv_heads;
     const int32_t q0 = __ldg(query_start_loc + seq);
