@@ -494,8 +494,9 @@ class DeviceStep:
             return
         if self.fused_append:
             rec("decode", 0)
+            # the tables are written by host copies only, never by the kernel before
             B.pa_decode_append(T["out"], T["q"], T["k_new"], T["v_new"], T["slots"], self.kcs[r], self.vcs[r], T["bt"],
-                               T["lens"], self.msl, wl.scale, self.ws, stream=s)
+                               T["lens"], self.msl, wl.scale, self.ws, stream=s, tables_ready=True)
             rec("decode", 1)
             return
         if self.has_new:

@@ -180,13 +180,23 @@ PA_API pa_status pa_decode(void* out, const void* q, const void* k_cache, const 
  * (skipped if negative) and attention uses the new rows at position seq_lens[i] - 1.
  * Arguments as for pa_decode_bs, plus k_new, v_new (16-byte aligned) and slot_mapping
  * (int64 [num_seqs], 8-byte aligned); workspace as for pa_decode.
+ *
+ * flags: 0 or PA_DECODE_TABLES_READY. With it the caller promises that the kernel launched
+ * just before this call on `stream` writes neither seq_lens nor block_table (they come from
+ * host copies or an earlier step); the fused kernel then scans the lengths and loads its first
+ * block ids while that kernel finishes, and waits for it only before touching the pool, the
+ * queries, the new rows, the output or the workspace. Any other flag bit returns
+ * PA_ERR_INVALID_ARG.
  */
+#define PA_DECODE_TABLES_READY 1u
+
 PA_API pa_status pa_decode_append(void* out, const void* q, const void* k_new, const void* v_new,
                                   const int64_t* slot_mapping, void* k_cache, void* v_cache,
                                   const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
                                   int32_t num_seqs, int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
                                   int32_t head_dim, int32_t num_blocks, int32_t block_size, float scale,
-                                  pa_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
+                                  pa_dtype dtype, void* workspace, size_t workspace_bytes, uint32_t flags,
+                                  void* stream);
 
 /* pa_decode with block_size (see the block-size variants above). */
 PA_API pa_status pa_decode_bs(void* out, const void* q, const void* k_cache, const void* v_cache,

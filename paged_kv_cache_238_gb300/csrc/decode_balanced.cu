@@ -270,7 +270,8 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
     int32_t max_blocks, const int32_t* __restrict__ seq_lens, int32_t S, int32_t num_kv_heads, int32_t G,
     int32_t num_blocks, int32_t sub_log2, float scale_log2, int32_t nst, uint32_t stage_bytes, BalWorkspace ws,
     uint32_t* err, const int4* __restrict__ k_new, const int4* __restrict__ v_new,
-    const int64_t* __restrict__ slot_mapping, int4* __restrict__ k_pool, int4* __restrict__ v_pool) {
+    const int64_t* __restrict__ slot_mapping, int4* __restrict__ k_pool, int4* __restrict__ v_pool,
+    int32_t tables_ready) {
     constexpr uint32_t kPage = kPageTokens * D * 2;
     constexpr uint32_t kHalves = D / 64;
     constexpr int KS = D / 16;  // k-steps over head_dim
@@ -295,8 +296,12 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
     const int32_t cap = table_tokens(max_blocks, sub_log2);
     const int32_t Hq = G * num_kv_heads;
 
-    // Inputs may come from the kernel before this one in the stream (programmatic launch).
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Inputs may come from the kernel before this one in the stream (programmatic launch). When
+    // the caller says that kernel writes neither seq_lens nor the block table (tables_ready),
+    // the lengths scan and the first block-id loads run before the wait, overlapping its tail;
+    // everything else (pool, queries, new rows, output, workspace) is touched after it.
+    auto dep_wait = [&]() { asm volatile("griddepcontrol.wait;" ::: "memory"); };
+    if (!tables_ready) dep_wait();
     // Let the next kernel's grid be launched now: its CTAs take an SM as soon as one of ours
     // leaves it (a second decode CTA does not fit beside this one) and wait there for this grid
     // to complete, so the launch latency hides behind our merge tail.
@@ -357,6 +362,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
     // are written here
     for (int32_t s = blockIdx.x; s < S; s += gridDim.x) {
         if (lens[s] != 0) continue;
+        if (tables_ready) dep_wait();
         uint32_t* z = reinterpret_cast<uint32_t*>(out + static_cast<int64_t>(s) * Hq * D);
         for (int32_t i = tid; i < Hq * D / 2; i += NTH) z[i] = 0u;
         if (append) {
@@ -409,6 +415,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
         int32_t id_nxt = n > 32 ? lane_row(1) : 0;
         Walker wi;
         wi.at(prefix, lens, S, num_kv_heads, a_w);
+        if (tables_ready) dep_wait();  // from here on: pool, queries, new rows, output
         // KV pages are read once per call: let them leave L2 first, ahead of the block table,
         // queries, lengths and this kernel's own code.
         const uint64_t kv_policy = l2_policy_evict_first();
@@ -688,6 +695,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
             for (int32_t u = consumed; u < issued; ++u) mbar_drain(&bars[u % nst], static_cast<uint32_t>(u / nst) & 1u);
         }
     }
+    if (tables_ready && n <= 0) dep_wait();  // warps without pages still merge and write
     __syncthreads();
     if (*abort_flag) return;
 
@@ -877,7 +885,7 @@ cudaError_t launch_impl(const DecodeArgs& a, const DecodePlan& plan, cudaStream_
                               block_size_log2(a.block_size) - 4, a.scale * kLog2e, plan.stages, plan.stage_bytes, ws,
                               a.err, static_cast<const int4*>(a.k_new), static_cast<const int4*>(a.v_new),
                               a.slot_mapping, static_cast<int4*>(const_cast<void*>(a.k_cache)),
-                              static_cast<int4*>(const_cast<void*>(a.v_cache)));
+                              static_cast<int4*>(const_cast<void*>(a.v_cache)), a.tables_ready ? 1 : 0);
 }
 
 // CTAs of the NW-warp kernel that fit on one SM with `smem` bytes of dynamic shared memory

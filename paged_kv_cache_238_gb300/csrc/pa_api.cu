@@ -316,7 +316,9 @@ PA_API pa_status pa_decode_append(void* out, const void* q, const void* k_new, c
                                   const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
                                   int32_t num_seqs, int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
                                   int32_t head_dim, int32_t num_blocks, int32_t block_size, float scale,
-                                  pa_dtype dtype, void* workspace, size_t workspace_bytes, void* stream) {
+                                  pa_dtype dtype, void* workspace, size_t workspace_bytes, uint32_t flags,
+                                  void* stream) {
+    if (flags & ~static_cast<uint32_t>(PA_DECODE_TABLES_READY)) return PA_ERR_INVALID_ARG;
     DecodeArgs a;
     pa_status st = prepare_decode(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens, num_seqs,
                                   max_seq_len, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale,
@@ -337,6 +339,7 @@ PA_API pa_status pa_decode_append(void* out, const void* q, const void* k_new, c
         a.k_new = k_new;
         a.v_new = v_new;
         a.slot_mapping = slot_mapping;
+        a.tables_ready = (flags & PA_DECODE_TABLES_READY) != 0;
         return launch_decode(a, plan, s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
     }
     if (launch_reshape_and_cache(ra, dev->info.num_sms, s) != cudaSuccess) return PA_ERR_CUDA;

@@ -68,6 +68,8 @@ struct DecodeArgs {
     const void* k_new = nullptr;
     const void* v_new = nullptr;
     const int64_t* slot_mapping = nullptr;
+    // the kernel before this one on the stream writes neither seq_lens nor block_table
+    bool tables_ready = false;
 };
 
 enum DecodePath : int {

@@ -230,6 +230,7 @@ def test_step_null_descriptor():
     (dict(D=96), B.PA_ERR_UNSUPPORTED),
     (dict(max_len=65), B.PA_ERR_INVALID_ARG),
     (dict(S=0, out=None, q=None, k_new=None), B.PA_OK),
+    (dict(flags=2), B.PA_ERR_INVALID_ARG),               # unknown flag bit
 ])
 def test_decode_append_rejects_bad_arguments(kw, expect):
     a = dict(out=FAKE, q=FAKE, k_new=FAKE, v_new=FAKE, slots=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, mb=4, lens=FAKE, S=2,
@@ -237,4 +238,4 @@ def test_decode_append_rejects_bad_arguments(kw, expect):
     a.update(kw)
     assert B.load().pa_decode_append(a["out"], a["q"], a["k_new"], a["v_new"], a["slots"], a["kc"], a["vc"], a["bt"],
                                      a["mb"], a["lens"], a["S"], a["max_len"], a["Hq"], a["Hkv"], a["D"], a["NB"],
-                                     a["bs"], 0.1, a["dt"], FAKE, 1 << 24, None) == expect
+                                     a["bs"], 0.1, a["dt"], FAKE, 1 << 24, a.get("flags", 0), None) == expect

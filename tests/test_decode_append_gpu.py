@@ -116,3 +116,28 @@ def test_decode_append_zero_sequences_is_a_no_op():
     B.pa_decode_append(dw.out[:0], dw.q[:0], dw.k_new[:0], dw.v_new[:0], dw.slot_mapping[:0], dw.k_cache,
                        dw.v_cache, dw.block_table[:0], dw.seq_lens[:0], 0, wl.scale, None)
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("G,H_kv", [(4, 8), (16, 2)])
+def test_decode_append_tables_ready_back_to_back(G, H_kv):
+    """PA_DECODE_TABLES_READY: the lengths scan and the first block ids are read before the
+    grid-dependency wait. Ten calls back to back on one stream (each a programmatic dependent
+    of the one before, all rewriting the same rows and reading the same tables) give the bits
+    of one call without the flag."""
+    wl = W.gqa_decode(seed=640)
+    wl = W.build_decode(641, wl.seq_lens, H_q=G * H_kv, H_kv=H_kv, D=128,
+                        num_blocks=int(np.sum(-(-wl.seq_lens.astype(np.int64) // 16))) + 2, dtype="bf16")
+    a = DeviceWorkload(wl)
+    _append(a)
+    ref_bits = to_host_bits(a.out)
+    b = DeviceWorkload(wl)
+    msl = int(wl.seq_lens.max())
+    ws = _ws(wl, b, msl)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for _ in range(10):
+            B.pa_decode_append(b.out, b.q, b.k_new, b.v_new, b.slot_mapping, b.k_cache, b.v_cache, b.block_table,
+                               b.seq_lens, msl, wl.scale, ws, stream=s, tables_ready=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_host_bits(b.out), ref_bits)
+    _check(b, f"tables ready G{G}")
