@@ -301,7 +301,7 @@ def build_mixed(seed: int, prior_lens, chunk_lens, decode_lens, H_q: int, H_kv: 
 
 
 # --------------------------------------------------------------------------------------
-# The five named workloads (seed = 1000 + workload number)
+# The five named workloads (seeds 1001 to 1005)
 # --------------------------------------------------------------------------------------
 
 def lognormal_lens(rng: np.random.Generator, n: int, mean: float = 195.0, sigma: float = 1.0,
@@ -365,4 +365,5 @@ def mixed_step(seed: int = 1005, n_prefill: int = 16, chunk: int = 512, n_decode
                        num_blocks=nb, dtype="bf16", name="mixed_step")
 
 
-WORKLOADS = {1: tiny_fp32, 2: gqa_decode, 3: prefix_sharing, 4: long_split_kv, 5: mixed_step}
+WORKLOADS = {"tiny_fp32": tiny_fp32, "gqa_decode": gqa_decode, "prefix_sharing": prefix_sharing,
+             "long_split_kv": long_split_kv, "mixed_step": mixed_step}

@@ -60,9 +60,9 @@ def check_pool(dw: DeviceWorkload, kc_ref, vc_ref):
 
 # ----------------------------------------------------------------------------- reshape_and_cache
 
-@pytest.mark.parametrize("cfg", [1, 2, 5])
-def test_reshape_and_cache_bit_exact(cfg):
-    dw = DeviceWorkload(W.WORKLOADS[cfg]())
+@pytest.mark.parametrize("name", ["tiny_fp32", "gqa_decode", "mixed_step"])
+def test_reshape_and_cache_bit_exact(name):
+    dw = DeviceWorkload(W.WORKLOADS[name]())
     run_reshape(dw)
     torch.cuda.synchronize()
     kc_ref, vc_ref = dw.host_pool_after_writes()
