@@ -24,11 +24,14 @@
  *   GQA                query head h reads kv head h / (num_q_heads / num_kv_heads)
  *
  * Conventions shared by every entry point:
- *   - Every pointer is a device pointer owned and allocated by the caller; the library
- *     allocates no device memory and keeps no per-call state. Pointers must be 16-byte
- *     aligned.
+ *   - Every pointer is a device pointer owned and allocated by the caller (the block
+ *     manager's calls, which take host arrays, excepted); the library allocates no device
+ *     memory at run time and keeps no per-call state. Per device it holds the error word, the
+ *     fixed scratch of pa_decode_noalloc, and pa_step's side stream and two events. Device
+ *     pointers must be 16-byte aligned unless an entry point states otherwise.
  *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL = legacy
- *     default stream). They never read device data on the host and never synchronise.
+ *     default stream). They never read device data on the host and never synchronise
+ *     (pa_get_device_errors excepted).
  *   - Arguments that the host can check (null pointers, sizes, head ratio, head_dim,
  *     dtype, workspace size, alignment) are checked before anything is launched; a bad
  *     one returns PA_ERR_INVALID_ARG or PA_ERR_UNSUPPORTED and launches nothing.
