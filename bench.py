@@ -357,16 +357,29 @@ def cpu_baseline(wl, budget_s: float = 10.0, value_key: str = "step") -> dict:
             break
     dt = time.perf_counter() - t0
     tokens = sd + (int(sub.query_start_loc[-1]) if sp else 0)
+    # the same oracle on one core, over a sixteenth of the sample (rate per sequence kept)
+    sd1, sp1 = (max(1, sd // 16) if sd else 0), (max(1, sp // 16) if sp else 0)
+    sub1 = _subset(wl, sd1, sp1)
+    t1 = time.perf_counter()
+    _oracle_pass(sub1, 1)
+    dt1 = time.perf_counter() - t1
+    tokens1 = sd1 + (int(sub1.query_start_loc[-1]) if sp1 else 0)
     res = {"unit": "TB/s", "cores": cores, "kind": "oracle",
            "sample": f"{passes} passes over {sd} decode + {sp} prefill sequences of one step "
                      f"(reshape_and_cache + attention, fp64) in {dt:.1f} s",
            "seqs_per_s": (sd + sp) * passes / dt, "tokens_per_s": tokens * passes / dt}
+    b1 = step_bytes(sub1)
     if value_key == "tokens":
         res["value"], res["unit"] = tokens * passes / dt, "tokens/s"
+        one_core = tokens1 / dt1
     elif value_key == "flops":
         res["value"], res["unit"] = b["prefill_flops"] * passes / dt / 1e12, "TFLOP/s"
+        one_core = b1["prefill_flops"] / dt1 / 1e12
     else:
         res["value"] = b["step"] * passes / dt / 1e12
+        one_core = b1["step"] / dt1 / 1e12
+    res["one_core"] = {"value": one_core, "sample": f"1 pass over {sd1} decode + {sp1} prefill sequences on 1 core "
+                                                    f"in {dt1:.2f} s"}
     return res
 
 
