@@ -26,11 +26,18 @@
 // Split-KV reduce, in three levels, all with the same log-sum-exp merge
 //   M = max_p m_p,  w_p = l_p 2^(m_p - M),  out = sum_p w_p o_p / sum_p w_p :
 //  1. a segment inside one warp's sub-slice is normalised and written from registers;
-//  2. pieces cut by warp boundaries meet in shared memory after one CTA barrier and are
-//     merged there by the warp at which the segment's run of pieces starts;
+//  2. pieces cut by warp boundaries meet in shared memory after one CTA barrier; the groups
+//     of pieces are listed (those also cut by the CTA range first) and shared out over the
+//     CTA's warps;
 //  3. segments cut by CTA boundaries leave one piece per CTA in the workspace; the warp that
 //     counts the last piece (device-scope acquire-release counter per segment) merges them
 //     and puts the counter back to zero.
+//
+// Variants: a block of 32, 64 or 128 tokens is walked as 2, 4 or 8 pages of 16 (sub_log2);
+// APPEND fuses the step's new-token write (the page holding position len - 1 brings the new
+// K/V rows, which the warp patches in and stores to the token's slot); a grid capped below
+// the SM count (decode beside prefill) runs 10 warps per CTA; tables_ready moves the lengths
+// scan and the first block-id loads before the grid-dependency wait.
 #include <cuda.h>  // CUtensorMap (type only)
 #include <math.h>
 
