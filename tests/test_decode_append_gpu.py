@@ -141,3 +141,17 @@ def test_decode_append_tables_ready_back_to_back(G, H_kv):
     torch.cuda.synchronize()
     assert np.array_equal(to_host_bits(b.out), ref_bits)
     _check(b, f"tables ready G{G}")
+
+
+@pytest.mark.slow
+def test_long_split_kv_through_decode_append_as_benchmarked():
+    """The long split-KV workload (8 x 32 768 keys, 64 q / 8 kv heads) through pa_decode_append
+    with PA_DECODE_TABLES_READY, as the benchmark launches it: every row against the oracle and
+    the pool bit-exact."""
+    wl = W.long_split_kv()
+    dw = DeviceWorkload(wl)
+    msl = int(wl.seq_lens.max())
+    B.pa_decode_append(dw.out, dw.q, dw.k_new, dw.v_new, dw.slot_mapping, dw.k_cache, dw.v_cache, dw.block_table,
+                       dw.seq_lens, msl, wl.scale, _ws(wl, dw, msl), tables_ready=True)
+    torch.cuda.synchronize()
+    _check(dw, "long split-KV through pa_decode_append")
