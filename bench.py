@@ -388,10 +388,11 @@ class DeviceStep:
     reshape_and_cache of the step's new tokens, then chunked prefill and decode attention."""
 
     def __init__(self, wl, dev, R: int, stream, whole_step: bool = False, decode_sms: int = 0,
-                 fuse_append: bool = False):
+                 fuse_append: bool = False, pool_ready: bool = False):
         import torch
         from paged_kv_cache_238_gb300 import binding as B
         self.B, self.wl, self.stream, self.R = B, wl, stream, R
+        self.pool_ready = pool_ready
         self.decode_sms = decode_sms
         kc0, vc0 = to_dev(wl.k_cache, dev), to_dev(wl.v_cache, dev)
         self.kcs = [kc0] + [kc0.clone() for _ in range(R - 1)]
@@ -509,7 +510,8 @@ class DeviceStep:
             rec("decode", 0)
             # the tables are written by host copies only, never by the kernel before
             B.pa_decode_append(T["out"], T["q"], T["k_new"], T["v_new"], T["slots"], self.kcs[r], self.vcs[r], T["bt"],
-                               T["lens"], self.msl, wl.scale, self.ws, stream=s, tables_ready=True)
+                               T["lens"], self.msl, wl.scale, self.ws, stream=s, tables_ready=True,
+                               pool_ready=self.pool_ready)
             rec("decode", 1)
             return
         if self.has_new:
@@ -557,7 +559,7 @@ def run_ours(args):
     R = args.replicas
     stream = torch.cuda.Stream(device=dev)
     step = DeviceStep(wl, dev, R, stream, whole_step=not args.sequential, decode_sms=args.decode_sms,
-                      fuse_append=not args.sequential)
+                      fuse_append=not args.sequential, pool_ready=not args.no_pool_ready)
     if step.fused_append:
         # one kernel writes the new tokens and attends: its algorithmic bytes are the decode's
         # plus the new rows read once from the input and written once (not read back)
@@ -862,6 +864,8 @@ def main(argv=None):
     ap.add_argument("--sequential", action="store_true",
                     help="one call per kernel: no pa_step (mixed step) and no pa_decode_append (decode step)")
     ap.add_argument("--decode-sms", type=int, default=0, help="pa_step: SMs held by decode (0 = 27/64 of them)")
+    ap.add_argument("--no-pool-ready", action="store_true",
+                    help="decode step without PA_DECODE_POOL_READY (first page copies after the grid-dependency wait)")
     args = ap.parse_args(argv)
     _, _, default_steps, default_replicas = WORKLOADS[args.workload]
     if args.steps is None:

@@ -184,14 +184,24 @@ PA_API pa_status pa_decode(void* out, const void* q, const void* k_cache, const 
  * Arguments as for pa_decode_bs, plus k_new, v_new (16-byte aligned) and slot_mapping
  * (int64 [num_seqs], 8-byte aligned); workspace as for pa_decode.
  *
- * flags: 0 or PA_DECODE_TABLES_READY. With it the caller promises that the kernel launched
- * just before this call on `stream` writes neither seq_lens nor block_table (they come from
- * host copies or an earlier step); the fused kernel then scans the lengths and loads its first
- * block ids while that kernel finishes, and waits for it only before touching the pool, the
- * queries, the new rows, the output or the workspace. Any other flag bit returns
- * PA_ERR_INVALID_ARG.
+ * flags: 0, or an OR of the bits below; any other bit returns PA_ERR_INVALID_ARG. The fused
+ * kernel is a programmatic launch: it may start while the kernel launched just before it on
+ * `stream` still runs, and it waits for that kernel to complete before it reads what the flags
+ * do not declare ready. It lets the next kernel start only after that wait, so every kernel
+ * before the previous one has completed when it starts.
+ *   PA_DECODE_TABLES_READY: the kernel launched just before this call writes neither seq_lens
+ *     nor block_table (they come from host copies or an earlier step). The kernel then scans
+ *     the lengths and loads its first block ids before the wait; the pool, the queries, the
+ *     new rows, the output and the workspace are touched after it.
+ *   PA_DECODE_POOL_READY (implies PA_DECODE_TABLES_READY): in addition, that kernel writes no
+ *     pool row this call reads (keys 0 .. seq_lens[i] - 2; this call writes the new rows
+ *     itself). In a model's decode step the kernel before attention produces q, k_new and
+ *     v_new, never the pool, so the promise holds there. The kernel then also starts its first
+ *     page copies before the wait; the queries, the new rows, the output and the workspace are
+ *     still touched after it.
  */
 #define PA_DECODE_TABLES_READY 1u
+#define PA_DECODE_POOL_READY 2u
 
 PA_API pa_status pa_decode_append(void* out, const void* q, const void* k_new, const void* v_new,
                                   const int64_t* slot_mapping, void* k_cache, void* v_cache,

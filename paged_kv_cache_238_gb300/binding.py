@@ -18,6 +18,7 @@ PA_F32, PA_BF16 = 0, 1
 PA_DEVERR_SLOT_RANGE, PA_DEVERR_BLOCK_RANGE, PA_DEVERR_LEN_RANGE, PA_DEVERR_WAIT_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 PA_DEVERR_APPEND_SLOT = 0x10
 PA_DECODE_TABLES_READY = 0x1
+PA_DECODE_POOL_READY = 0x2
 BLOCK_SIZE = 16
 
 #: every symbol that include/pa.h declares
@@ -231,11 +232,13 @@ def pa_decode_bs(out, q, k_cache, v_cache, block_table, seq_lens, max_seq_len: i
 
 
 def pa_decode_append(out, q, k_new, v_new, slot_mapping, k_cache, v_cache, block_table, seq_lens,
-                     max_seq_len: int, scale: float, workspace=None, stream=None, tables_ready: bool = False) -> None:
+                     max_seq_len: int, scale: float, workspace=None, stream=None, tables_ready: bool = False,
+                     pool_ready: bool = False) -> None:
     """Decode step with its new tokens (C ABI pa_decode_append): k_new, v_new [S, H_kv, D] of
     sequence i's token at position seq_lens[i] - 1 are written to slot_mapping[i] ([S] int64)
     and attended to; one launch on the bf16 persistent path. tables_ready: the kernel launched
-    just before on the stream writes neither seq_lens nor block_table (PA_DECODE_TABLES_READY)."""
+    just before on the stream writes neither seq_lens nor block_table (PA_DECODE_TABLES_READY);
+    pool_ready: nor the pool rows this call reads (PA_DECODE_POOL_READY, implies tables_ready)."""
     _need_cuda(out, q, k_new, v_new, slot_mapping, k_cache, v_cache, block_table, seq_lens, workspace)
     S, H_q, D = q.shape
     NB, H_kv, BS = k_cache.shape[0], k_cache.shape[1], k_cache.shape[2]
@@ -243,7 +246,8 @@ def pa_decode_append(out, q, k_new, v_new, slot_mapping, k_cache, v_cache, block
     _check("pa_decode_append", load().pa_decode_append(
         _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
         _ptr(block_table), block_table.shape[1], _ptr(seq_lens), S, int(max_seq_len), H_q, H_kv, D, NB, int(BS),
-        float(scale), _dtype_code(q), _ptr(workspace), ws_bytes, PA_DECODE_TABLES_READY if tables_ready else 0,
+        float(scale), _dtype_code(q), _ptr(workspace), ws_bytes,
+        (PA_DECODE_TABLES_READY if tables_ready else 0) | (PA_DECODE_POOL_READY if pool_ready else 0),
         _stream(stream)))
 
 

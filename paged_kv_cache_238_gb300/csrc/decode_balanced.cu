@@ -43,8 +43,13 @@
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
+#include "pa_trace.cuh"
 
 namespace pa {
+#ifdef PA_TRACE
+static __device__ uint64_t g_trace[kTraceWords];
+static __device__ uint32_t g_trace_counter;
+#endif
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -278,7 +283,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
     int32_t num_blocks, int32_t sub_log2, float scale_log2, int32_t nst, uint32_t stage_bytes, BalWorkspace ws,
     uint32_t* err, const int4* __restrict__ k_new, const int4* __restrict__ v_new,
     const int64_t* __restrict__ slot_mapping, int4* __restrict__ k_pool, int4* __restrict__ v_pool,
-    int32_t tables_ready) {
+    int32_t tables_ready, int32_t pool_ready) {
     constexpr uint32_t kPage = kPageTokens * D * 2;
     constexpr uint32_t kHalves = D / 64;
     constexpr int KS = D / 16;  // k-steps over head_dim
@@ -302,17 +307,29 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
     const int32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t cap = table_tokens(max_blocks, sub_log2);
     const int32_t Hq = G * num_kv_heads;
+    PA_TRACE_DECL
+    PA_TRACE_BEGIN(g_trace_counter);
+    PA_TRACE_STAMP(g_trace, 0);
 
     // Inputs may come from the kernel before this one in the stream (programmatic launch). When
     // the caller says that kernel writes neither seq_lens nor the block table (tables_ready),
     // the lengths scan and the first block-id loads run before the wait, overlapping its tail;
     // everything else (pool, queries, new rows, output, workspace) is touched after it.
-    auto dep_wait = [&]() { asm volatile("griddepcontrol.wait;" ::: "memory"); };
+    // Right after its wait each thread also lets the next kernel's grid be launched: its CTAs
+    // take an SM as soon as one of ours leaves it (a second decode CTA does not fit beside this
+    // one) and wait there for this grid to complete, so the launch latency hides behind our
+    // merge tail. Triggering only after the wait means that every kernel before this one has
+    // completed when the next one starts.
+    auto dep_wait = [&]() {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    };
+    // The tensor maps are kernel parameters, which no earlier kernel writes: fetch them now.
+    if (tid == 0) {
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+    }
     if (!tables_ready) dep_wait();
-    // Let the next kernel's grid be launched now: its CTAs take an SM as soon as one of ours
-    // leaves it (a second decode CTA does not fit beside this one) and wait there for this grid
-    // to complete, so the launch latency hides behind our merge tail.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // ---- prologue: clamped lengths and units per sequence, block-wide exclusive scan -------
     {
@@ -355,6 +372,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
         if (tid == NTH - 1) prefix[S] = base + incl;
         __syncthreads();
     }
+    PA_TRACE_STAMP(g_trace, 1);
 
     const int64_t U = prefix[S];
     const int64_t C = gridDim.x;
@@ -422,58 +440,99 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
         int32_t id_nxt = n > 32 ? lane_row(1) : 0;
         Walker wi;
         wi.at(prefix, lens, S, num_kv_heads, a_w);
-        if (tables_ready) dep_wait();  // from here on: pool, queries, new rows, output
         // KV pages are read once per call: let them leave L2 first, ahead of the block table,
         // queries, lengths and this kernel's own code.
         const uint64_t kv_policy = l2_policy_evict_first();
+        const uint32_t qbytes = static_cast<uint32_t>(G) * D * 2u;
 
-        auto issue = [&](int32_t t) {  // warp-uniform
+        // Pool row of unit t's page (block ids fetched 32 units ahead); warp-uniform.
+        auto page_row = [&](int32_t t) -> int32_t {
             if ((t >> 5) == kc + 1) {
                 ++kc;
                 id_cur = id_nxt;
                 id_nxt = 32 * (kc + 1) < n ? lane_row(kc + 1) : 0;
             }
-            const int32_t row = __shfl_sync(0xffffffffu, id_cur, t & 31);
-            const bool seg_first = (t == 0) || (wi.j == 0);
-            const bool new_row = append && wi.j == wi.np - 1;  // the page that holds position len - 1
-            if (lane == 0 && !*abort_flag) {
-                const int32_t st = t % nst;
-                uint8_t* stage = ring + static_cast<uint32_t>(st) * stage_bytes;
-                const uint32_t qbytes = static_cast<uint32_t>(G) * D * 2u;
-                if (new_row) {
-                    // behind the query rows: the token's K row, V row, slot and the page's pool row
-                    uint8_t* ex = stage + 2u * kPage + qbytes;
-                    *reinterpret_cast<int32_t*>(ex + 4u * D + 8u) = row;
-                    async_copy8_tracked(ex + 4u * D, slot_mapping + wi.s, &bars[st]);
-                    const int64_t r = static_cast<int64_t>(wi.s) * num_kv_heads + wi.h;
-                    mbar_arrive_expect_tx(&bars[st], 2u * kPage + (seg_first ? qbytes : 0u) + 4u * D);
-                    bulk_copy_g2s(ex, k_new + r * CPR, D * 2u, &bars[st]);
-                    bulk_copy_g2s(ex + D * 2u, v_new + r * CPR, D * 2u, &bars[st]);
-                } else {
-                    mbar_arrive_expect_tx(&bars[st], 2u * kPage + (seg_first ? qbytes : 0u));
-                }
-                if constexpr (kHalves == 2) {  // both 64-column halves in one box
-                    tma_load_3d_hint(stage, &tm_k, 0, row, 0, &bars[st], kv_policy);
-                    tma_load_3d_hint(stage + kPage, &tm_v, 0, row, 0, &bars[st], kv_policy);
-                } else {
-                    tma_load_2d_hint(stage, &tm_k, 0, row, &bars[st], kv_policy);
-                    tma_load_2d_hint(stage + kPage, &tm_v, 0, row, &bars[st], kv_policy);
-                }
-                if (seg_first) {
-                    bulk_copy_g2s(stage + 2u * kPage, q + (static_cast<int64_t>(wi.s) * Hq + wi.h * G) * D, qbytes,
-                                  &bars[st]);
-                }
+            return __shfl_sync(0xffffffffu, id_cur, t & 31);
+        };
+        // Bytes that arrive in a stage besides the K and V pages: the segment's query rows with
+        // its first page, the new token's rows with the page that holds position len - 1.
+        auto extra_bytes = [&](int32_t t, const Walker& w) -> uint32_t {
+            const bool seg_first = (t == 0) || (w.j == 0);
+            const bool new_row = append && w.j == w.np - 1;
+            return (seg_first ? qbytes : 0u) + (new_row ? 4u * D : 0u);
+        };
+        // The page copies of unit t (lane 0). With `arrive` the stage's single arrival is made
+        // here together with every byte it expects; without it only the pages' bytes are
+        // announced, and issue_rest() arrives later.
+        auto issue_pages = [&](int32_t t, int32_t row, const Walker& w, bool arrive) {
+            const int32_t st = t % nst;
+            uint8_t* stage = ring + static_cast<uint32_t>(st) * stage_bytes;
+            if (append && w.j == w.np - 1)  // the page's pool row, behind the query rows and new K/V
+                *reinterpret_cast<int32_t*>(stage + 2u * kPage + qbytes + 4u * D + 8u) = row;
+            if (arrive) mbar_arrive_expect_tx(&bars[st], 2u * kPage + extra_bytes(t, w));
+            else mbar_expect_tx(&bars[st], 2u * kPage);
+            if constexpr (kHalves == 2) {  // both 64-column halves in one box
+                tma_load_3d_hint(stage, &tm_k, 0, row, 0, &bars[st], kv_policy);
+                tma_load_3d_hint(stage + kPage, &tm_v, 0, row, 0, &bars[st], kv_policy);
+            } else {
+                tma_load_2d_hint(stage, &tm_k, 0, row, &bars[st], kv_policy);
+                tma_load_2d_hint(stage + kPage, &tm_v, 0, row, &bars[st], kv_policy);
             }
+        };
+        // The rest of unit t's stage (lane 0): the segment's query rows, the new token's K/V rows
+        // and its slot; `arrive` makes the stage's arrival (pages already announced).
+        auto issue_rest = [&](int32_t t, const Walker& w, bool arrive) {
+            const int32_t st = t % nst;
+            uint8_t* stage = ring + static_cast<uint32_t>(st) * stage_bytes;
+            if (arrive) mbar_arrive_expect_tx(&bars[st], extra_bytes(t, w));
+            if (append && w.j == w.np - 1) {
+                uint8_t* ex = stage + 2u * kPage + qbytes;
+                async_copy8_tracked(ex + 4u * D, slot_mapping + w.s, &bars[st]);
+                const int64_t r = static_cast<int64_t>(w.s) * num_kv_heads + w.h;
+                bulk_copy_g2s(ex, k_new + r * CPR, D * 2u, &bars[st]);
+                bulk_copy_g2s(ex + D * 2u, v_new + r * CPR, D * 2u, &bars[st]);
+            }
+            if ((t == 0) || (w.j == 0))
+                bulk_copy_g2s(stage + 2u * kPage, q + (static_cast<int64_t>(w.s) * Hq + w.h * G) * D, qbytes, &bars[st]);
+        };
+        auto issue = [&](int32_t t) {  // warp-uniform
+            const int32_t row = page_row(t);
+            if (lane == 0 && !*abort_flag) {
+                issue_pages(t, row, wi, true);
+                issue_rest(t, wi, false);
+            }
+            if (t < 8) PA_TRACE_STAMP(g_trace, 24 + t);
             wi.advance(prefix, lens, S, num_kv_heads);
             issued = t + 1;
         };
 
-        if (lane == 0) {
-            prefetch_tensormap(&tm_k);
-            prefetch_tensormap(&tm_v);
-        }
         const int32_t pre = min(nst, n);
-        for (int32_t t = 0; t < pre; ++t) issue(t);
+        if (pool_ready) {
+            // The pool pages do not come from the kernel before this one: start the first
+            // stages' page copies now and only the rest of each stage after the wait. Each
+            // stage's phase completes only after its arrival (made after the wait), whatever
+            // the order in which the bytes land.
+            for (int32_t t = 0; t < pre; ++t) {
+                const int32_t row = page_row(t);
+                if (lane == 0) issue_pages(t, row, wi, false);
+                if (t < 8) PA_TRACE_STAMP(g_trace, 24 + t);
+                wi.advance(prefix, lens, S, num_kv_heads);
+            }
+            dep_wait();  // from here on: queries, new rows, output, workspace
+            PA_TRACE_STAMP(g_trace, 2);
+            Walker wq;
+            wq.at(prefix, lens, S, num_kv_heads, a_w);
+            for (int32_t t = 0; t < pre; ++t) {
+                if (lane == 0) issue_rest(t, wq, true);
+                wq.advance(prefix, lens, S, num_kv_heads);
+            }
+            issued = pre;
+        } else {
+            if (tables_ready) dep_wait();  // from here on: pool, queries, new rows, output
+            PA_TRACE_STAMP(g_trace, 2);
+            for (int32_t t = 0; t < pre; ++t) issue(t);
+        }
+        PA_TRACE_STAMP(g_trace, 3);
 
         Walker wc;
         wc.at(prefix, lens, S, num_kv_heads, a_w);
@@ -500,6 +559,8 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
                 break;
             }
             consumed = t + 1;
+            if (t == 0) PA_TRACE_STAMP(g_trace, 4);
+            if (t < 8) PA_TRACE_STAMP(g_trace, 16 + t);
             uint8_t* stage = ring + static_cast<uint32_t>(st) * stage_bytes;
             const uint32_t k_u32 = ring_u32 + static_cast<uint32_t>(st) * stage_bytes;
             const uint32_t v_u32 = k_u32 + kPage;
@@ -697,6 +758,8 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
             if (t + nst < n) issue(t + nst);
             wc.advance(prefix, lens, S, num_kv_heads);
         }
+        PA_TRACE_STAMP(g_trace, 5);
+        PA_TRACE_AT(g_trace, 12, static_cast<uint64_t>(n));
         // after an abort: let the copies already issued land before the CTA can exit
         if (consumed < issued && lane == 0) {
             for (int32_t u = consumed; u < issued; ++u) mbar_drain(&bars[u % nst], static_cast<uint32_t>(u / nst) & 1u);
@@ -704,6 +767,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
     }
     if (tables_ready && n <= 0) dep_wait();  // warps without pages still merge and write
     __syncthreads();
+    PA_TRACE_STAMP(g_trace, 6);
     if (*abort_flag) return;
 
     // ---- level 2: merge the pieces of segments cut between this CTA's warps ----------------
@@ -733,7 +797,11 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
         }
     }
     __syncthreads();
+    PA_TRACE_STAMP(g_trace, 7);
     const int32_t n_cross = gcount[0], n_groups = gcount[0] + gcount[1];
+#ifdef PA_TRACE
+    uint64_t tr_groups = 0, tr_l3 = 0;
+#endif
     for (int32_t gi = warp; gi < n_groups; gi += NW) {
         const int32_t owner = glist[gi < n_cross ? gi : 2 * NW - 1 - (gi - n_cross)];
         const int32_t ow = owner >> 1, s0 = owner & 1;
@@ -841,13 +909,24 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
             if (lane == 0) last = count_piece(ws.counter + seg) == expected - 1;
             last = __shfl_sync(0xffffffffu, last, 0);
             __syncwarp();  // lane 0's acquire precedes every lane's loads of other pieces
+            PA_TRACE_STAMP(g_trace, 9);
+#ifdef PA_TRACE
+            tr_l3 += last ? 2 : 1;
+#endif
             if (last) {
                 merge_pieces<D>(out + (static_cast<int64_t>(s) * Hq + h * G) * D, seg_a, c_first, c_last, U, C, G, ws,
                                 lane);
                 if (lane == 0) ws.counter[seg] = 0;
+                PA_TRACE_STAMP(g_trace, 10);
             }
         }
+#ifdef PA_TRACE
+        ++tr_groups;
+#endif
     }
+    PA_TRACE_STAMP(g_trace, 8);
+    PA_TRACE_AT(g_trace, 13, tr_groups);
+    PA_TRACE_AT(g_trace, 14, tr_l3);
 }
 
 template <int D, int NW, int NH, bool APPEND>
@@ -892,7 +971,8 @@ cudaError_t launch_impl(const DecodeArgs& a, const DecodePlan& plan, cudaStream_
                               block_size_log2(a.block_size) - 4, a.scale * kLog2e, plan.stages, plan.stage_bytes, ws,
                               a.err, static_cast<const int4*>(a.k_new), static_cast<const int4*>(a.v_new),
                               a.slot_mapping, static_cast<int4*>(const_cast<void*>(a.k_cache)),
-                              static_cast<int4*>(const_cast<void*>(a.v_cache)), a.tables_ready ? 1 : 0);
+                              static_cast<int4*>(const_cast<void*>(a.v_cache)), a.tables_ready ? 1 : 0,
+                              a.pool_ready ? 1 : 0);
 }
 
 // CTAs of the NW-warp kernel that fit on one SM with `smem` bytes of dynamic shared memory
@@ -980,3 +1060,20 @@ cudaError_t launch_decode_balanced(const DecodeArgs& a, const DecodePlan& plan, 
 }
 
 }  // namespace pa
+
+#ifdef PA_TRACE
+// Profiling builds only: copy the timeline ring to the host / clear it (current device).
+extern "C" PA_API int pa_trace_read(void* host, size_t bytes) {
+    if (bytes > sizeof(pa::g_trace)) bytes = sizeof(pa::g_trace);
+    return static_cast<int>(cudaMemcpyFromSymbol(host, pa::g_trace, bytes));
+}
+extern "C" PA_API int pa_trace_reset() {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, pa::g_trace);
+    if (e == cudaSuccess) e = cudaMemset(p, 0, sizeof(pa::g_trace));
+    if (e == cudaSuccess) e = cudaGetSymbolAddress(&p, pa::g_trace_counter);
+    if (e == cudaSuccess) e = cudaMemset(p, 0, sizeof(uint32_t));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    return static_cast<int>(e);
+}
+#endif

@@ -318,7 +318,7 @@ PA_API pa_status pa_decode_append(void* out, const void* q, const void* k_new, c
                                   int32_t head_dim, int32_t num_blocks, int32_t block_size, float scale,
                                   pa_dtype dtype, void* workspace, size_t workspace_bytes, uint32_t flags,
                                   void* stream) {
-    if (flags & ~static_cast<uint32_t>(PA_DECODE_TABLES_READY)) return PA_ERR_INVALID_ARG;
+    if (flags & ~static_cast<uint32_t>(PA_DECODE_TABLES_READY | PA_DECODE_POOL_READY)) return PA_ERR_INVALID_ARG;
     DecodeArgs a;
     pa_status st = prepare_decode(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens, num_seqs,
                                   max_seq_len, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale,
@@ -339,7 +339,8 @@ PA_API pa_status pa_decode_append(void* out, const void* q, const void* k_new, c
         a.k_new = k_new;
         a.v_new = v_new;
         a.slot_mapping = slot_mapping;
-        a.tables_ready = (flags & PA_DECODE_TABLES_READY) != 0;
+        a.pool_ready = (flags & PA_DECODE_POOL_READY) != 0;
+        a.tables_ready = a.pool_ready || (flags & PA_DECODE_TABLES_READY) != 0;
         return launch_decode(a, plan, s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
     }
     if (launch_reshape_and_cache(ra, dev->info.num_sms, s) != cudaSuccess) return PA_ERR_CUDA;

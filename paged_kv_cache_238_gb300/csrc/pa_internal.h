@@ -70,6 +70,8 @@ struct DecodeArgs {
     const int64_t* slot_mapping = nullptr;
     // the kernel before this one on the stream writes neither seq_lens nor block_table
     bool tables_ready = false;
+    // ... nor the pool rows this call reads (implies tables_ready)
+    bool pool_ready = false;
 };
 
 enum DecodePath : int {

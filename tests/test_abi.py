@@ -230,7 +230,7 @@ def test_step_null_descriptor():
     (dict(D=96), B.PA_ERR_UNSUPPORTED),
     (dict(max_len=65), B.PA_ERR_INVALID_ARG),
     (dict(S=0, out=None, q=None, k_new=None), B.PA_OK),
-    (dict(flags=2), B.PA_ERR_INVALID_ARG),               # unknown flag bit
+    (dict(flags=4), B.PA_ERR_INVALID_ARG),               # unknown flag bit
 ])
 def test_decode_append_rejects_bad_arguments(kw, expect):
     a = dict(out=FAKE, q=FAKE, k_new=FAKE, v_new=FAKE, slots=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, mb=4, lens=FAKE, S=2,

@@ -118,12 +118,14 @@ def test_decode_append_zero_sequences_is_a_no_op():
     torch.cuda.synchronize()
 
 
+@pytest.mark.parametrize("pool_ready", [False, True])
 @pytest.mark.parametrize("G,H_kv", [(4, 8), (16, 2)])
-def test_decode_append_tables_ready_back_to_back(G, H_kv):
+def test_decode_append_tables_ready_back_to_back(G, H_kv, pool_ready):
     """PA_DECODE_TABLES_READY: the lengths scan and the first block ids are read before the
-    grid-dependency wait. Ten calls back to back on one stream (each a programmatic dependent
-    of the one before, all rewriting the same rows and reading the same tables) give the bits
-    of one call without the flag."""
+    grid-dependency wait (with PA_DECODE_POOL_READY the first page copies too). Ten calls back
+    to back on one stream (each a programmatic dependent of the one before, all rewriting the
+    same new rows, which no call reads from the pool, and reading the same tables and keys)
+    give the bits of one call without the flags."""
     wl = W.gqa_decode(seed=640)
     wl = W.build_decode(641, wl.seq_lens, H_q=G * H_kv, H_kv=H_kv, D=128,
                         num_blocks=int(np.sum(-(-wl.seq_lens.astype(np.int64) // 16))) + 2, dtype="bf16")
@@ -137,10 +139,10 @@ def test_decode_append_tables_ready_back_to_back(G, H_kv):
     with torch.cuda.stream(s):
         for _ in range(10):
             B.pa_decode_append(b.out, b.q, b.k_new, b.v_new, b.slot_mapping, b.k_cache, b.v_cache, b.block_table,
-                               b.seq_lens, msl, wl.scale, ws, stream=s, tables_ready=True)
+                               b.seq_lens, msl, wl.scale, ws, stream=s, tables_ready=True, pool_ready=pool_ready)
     torch.cuda.synchronize()
     assert np.array_equal(to_host_bits(b.out), ref_bits)
-    _check(b, f"tables ready G{G}")
+    _check(b, f"tables ready G{G}" + (" pool ready" if pool_ready else ""))
 
 
 @pytest.mark.slow
