@@ -80,3 +80,23 @@ def test_noalloc_rejects_shapes_beyond_the_fixed_scratch():
     st = lib.pa_decode_noalloc(p, p, p, p, p, msl // 16, p, S, msl, H_q, H_kv, D, 1024, ctypes.c_float(0.1),
                                B.PA_BF16, None)
     assert st == B.PA_ERR_UNSUPPORTED
+
+
+def test_noalloc_general_path_then_grouped_path_matches_oracle():
+    """The scratch keeps what the previous call left: an fp32 call (the general path writes
+    plain partial results all over it) followed by a bf16 grouped call, whose cross-CTA merges
+    count finished pieces in the scratch's leading words, must still give the oracle's result,
+    because each call clears those counters before launching."""
+    import oracle
+    first = W.build_decode(92, [2048, 1500, 3000, 77], H_q=8, H_kv=8, D=128, num_blocks=500, dtype="f32",
+                           new_token=False)
+    d1 = DeviceWorkload(first)
+    _noalloc_call(d1, int(first.seq_lens.max()))
+    second = W.build_decode(93, [900, 1300, 40, 2600, 5, 610], H_q=32, H_kv=8, D=128, num_blocks=800,
+                            dtype="bf16", new_token=False)
+    d2 = DeviceWorkload(second)
+    got = _noalloc_call(d2, int(second.seq_lens.max()))
+    ref = oracle.attention(second.q, second.k_cache, second.v_cache, second.block_table, second.seq_lens,
+                           second.scale)
+    assert_close(got, ref, "bf16", "grouped call after a general-path call")
+    assert B.pa_get_device_errors(clear=True) == 0
