@@ -124,11 +124,14 @@ PA_API pa_status pa_reshape_and_cache_bs(const void* k, const void* v, void* k_c
 
 /*
  * pa_decode_workspace_size: bytes of device scratch that pa_decode needs for this shape on
- * the current device (split-KV partial results and one merge counter per (sequence, kv
- * head)). The caller allocates it and zero-fills it once before its first use; every call
- * that completes without a device error leaves it zero-filled again, so the same buffer
- * serves any number of later calls (and CUDA-graph replays) without re-initialisation.
- * After a call that raised PA_DEVERR_WAIT_TIMEOUT, zero-fill it again. Calls that use the
+ * the current device (split-KV partial results; on the bf16 path for groups of 4..16 q heads
+ * per kv head, also one merge counter per (sequence, kv head) at its start). The caller
+ * allocates it and zero-fills it once before its first use. On that bf16 path every call
+ * that completes without a device error puts the counters back to zero, so the same buffer
+ * serves any number of later calls (and CUDA-graph replays) without re-initialisation. The
+ * general path (fp32, or fewer than 4 q heads per kv head) writes plain partial results over
+ * the whole buffer: zero-fill it again before a bf16 grouped call reuses a buffer that the
+ * general path used, and after a call that raised PA_DEVERR_WAIT_TIMEOUT. Calls that use the
  * same workspace must not overlap on the GPU.
  */
 PA_API size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
