@@ -615,11 +615,16 @@ def run_ours(args):
 
     # ---- e2e graph: pinned host inputs in, results out, every step ------------------------
     # The step's inputs and outputs are packed in one device buffer each (DeviceStep), so a
-    # step moves them with one copy each way. Two buffer sets alternate: step i+1's inputs
-    # travel host -> device on one copy stream while step i computes, and step i's outputs
-    # travel back on another once it is done (the two directions use separate copy engines);
-    # every step's copies are inside the timed region.
-    step.add_buffer()
+    # step moves them with one copy each way. Steps go in blocks of EB with their own buffer
+    # sets, two groups of sets alternating: block j+1's inputs travel host -> device on one
+    # copy stream while block j computes, and block j's outputs travel back on another once it
+    # is done (the two directions use separate copy engines). Inside a block the kernels follow
+    # one another with nothing between them, so each may launch early under the one before
+    # (programmatic launch); only the wait on a block's inputs sits between blocks. Every
+    # step's copies are inside the timed region.
+    EB = max(1, min(chunk, args.e2e_block))
+    for _ in range(2 * EB - 1):
+        step.add_buffer()
     h_in = step.in_arena.cpu().pin_memory()
     h_out = torch.empty(step.out_arena.shape, dtype=torch.uint8, pin_memory=True)
     h2d = h_in.numel()
@@ -632,27 +637,36 @@ def run_ours(args):
         start.record(stream)
         s_in.wait_event(start)
         s_out.wait_event(start)
-        copied, done, sent = [ev() for _ in range(n)], [ev() for _ in range(n)], [ev() for _ in range(n)]
-        with torch.cuda.stream(s_in):
-            step.in_arenas[0].copy_(h_in, non_blocking=True)
-            copied[0].record(s_in)
-        for i in range(n):
-            b = i % 2
-            stream.wait_event(copied[i])      # step i's inputs landed
-            if i >= 2:
-                stream.wait_event(sent[i - 2])  # step i-2's outputs (same buffer set) have left
-            step(i, buf=b)
-            done[i].record(stream)
-            if i + 1 < n:
-                with torch.cuda.stream(s_in):
-                    if i >= 1:
-                        s_in.wait_event(done[i - 1])  # buffer set (i + 1) % 2 is free again
-                    step.in_arenas[(i + 1) % 2].copy_(h_in, non_blocking=True)
-                    copied[i + 1].record(s_in)
+        blocks = [list(range(j, min(n, j + EB))) for j in range(0, n, EB)]
+        nb = len(blocks)
+        copied, done, sent = [ev() for _ in range(nb)], [ev() for _ in range(nb)], [ev() for _ in range(nb)]
+
+        def bufs(j):
+            return [(j % 2) * EB + k for k in range(len(blocks[j]))]
+
+        def send_inputs(j):
+            with torch.cuda.stream(s_in):
+                if j >= 2:
+                    s_in.wait_event(done[j - 2])  # block j-2 (same buffer group) has read its inputs
+                for b in bufs(j):
+                    step.in_arenas[b].copy_(h_in, non_blocking=True)
+                copied[j].record(s_in)
+
+        send_inputs(0)
+        for j in range(nb):
+            if j + 1 < nb:
+                send_inputs(j + 1)
+            stream.wait_event(copied[j])          # block j's inputs landed
+            if j >= 2:
+                stream.wait_event(sent[j - 2])    # block j-2's outputs (same buffer group) have left
+            for i, b in zip(blocks[j], bufs(j)):
+                step(i, buf=b)
+            done[j].record(stream)
             with torch.cuda.stream(s_out):
-                s_out.wait_event(done[i])
-                h_out.copy_(step.out_arenas[b], non_blocking=True)
-                sent[i].record(s_out)
+                s_out.wait_event(done[j])
+                for b in bufs(j):
+                    h_out.copy_(step.out_arenas[b], non_blocking=True)
+                sent[j].record(s_out)
         for s_ in (s_in, s_out):
             end = ev()
             end.record(s_)
@@ -669,21 +683,39 @@ def run_ours(args):
     g_e2e_rem = capture_e2e(rem) if rem else None
 
     def timed(gm, gr):
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        """The K-step graph(s) replayed back to back, at least args.min_replays times and for
+        at least args.min_timed_ms in all, each replay between its own pair of events: the
+        median replay (K steps), max over ranks, and the number of replays."""
+        def run_once(evs):
+            with torch.cuda.stream(stream):
+                evs[0].record(stream)
+                for _ in range(n_main):
+                    gm.replay()
+                if gr is not None:
+                    gr.replay()
+                evs[1].record(stream)
+
+        probe = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        run_once(probe)
+        torch.cuda.synchronize()
+        reps = max(args.min_replays, int(np.ceil(args.min_timed_ms / max(probe[0].elapsed_time(probe[1]), 1e-3))))
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
         with torch.cuda.stream(stream):
-            t0.record(stream)
-            for _ in range(n_main):
-                gm.replay()
-            if gr is not None:
-                gr.replay()
-            t1.record(stream)
+            evs[0].record(stream)
+            for r in range(reps):
+                for _ in range(n_main):
+                    gm.replay()
+                if gr is not None:
+                    gr.replay()
+                evs[r + 1].record(stream)
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
-        return max_over_ranks(t0.elapsed_time(t1), world, dev)
+        per = [evs[r].elapsed_time(evs[r + 1]) for r in range(reps)]
+        return max_over_ranks(float(np.median(per)), world, dev), reps, evs[0].elapsed_time(evs[-1])
 
     sampler = ClockSampler(local)
     sampler.start()
@@ -693,13 +725,13 @@ def run_ours(args):
         while time.perf_counter() < t_end:
             g_main.replay()
             stream.synchronize()
-    ms_total = timed(g_main, g_rem)
+    ms_total, reps, ms_region = timed(g_main, g_rem)
     clocks = sampler.stop()
     # per-kernel durations from the sampled steps of the last replay of the main graph (inside
     # the timed region)
     kern_ms = {k: sum(e[k][0].elapsed_time(e[k][1]) for e in ev_steps.values()) / len(ev_steps)
                for k in step.kernels}
-    ms_e2e = timed(g_e2e, g_e2e_rem)
+    ms_e2e, reps_e2e, _ = timed(g_e2e, g_e2e_rem)
     assert B.pa_get_device_errors(clear=True) == 0
 
     ms_step = ms_total / K
@@ -757,6 +789,8 @@ def run_ours(args):
                          f"{R * nbytes['kv_unique'] / 1e6:.0f} MB of distinct KV touched per rotation "
                          f"(L2 {L2_BYTES / 1e6:.0f} MB)",
                    "graph": f"{n_main} x {chunk}-step CUDA graph" + (f" + {rem}-step graph" if rem else ""),
+                   "timing": f"median over {reps} back-to-back replays of the {K}-step graph(s), each between "
+                             f"its own event pair ({ms_region:.1f} ms timed in all); e2e: median over {reps_e2e}",
                    "kernel_timing": (f"one kernel per step: the event pair around the {K}-step timed region over K "
                                      f"(us_single_launch: pairs around the kernel of every {sample}th step)")
                    if len(step.kernels) == 1 else
@@ -766,10 +800,11 @@ def run_ours(args):
         "seqs_per_s": round(n_seqs * world / (ms_step * 1e-3), 1),
         "tokens_per_s": round(tokens * world / (ms_step * 1e-3), 1),
         "e2e": {"value": round(e2e_value, nd), "unit": unit, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e / K, 6)},
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e / K, 6),
+                "blocks": f"{EB} steps per input/output copy group, two groups alternating"},
         "roofline": roof,
         "kernels": kernels,
-        "gpu_launches": launches_per_step * K,
+        "gpu_launches": launches_per_step * K * reps,
         "clocks": {k: clocks[k] for k in ("sm_mhz", "sm_max_mhz", "reasons")},
     }
     if step.fused_append:
@@ -857,6 +892,9 @@ def main(argv=None):
     ap.add_argument("--graph-chunk", type=int, default=500, help="steps per captured graph")
     ap.add_argument("--event-every", type=int, default=50, help="time each kernel on every Nth step of a graph")
     ap.add_argument("--preheat-s", type=float, default=1.0)
+    ap.add_argument("--min-replays", type=int, default=20, help="timed replays of the K-step graph (at least)")
+    ap.add_argument("--e2e-block", type=int, default=8, help="e2e: steps per input/output copy group")
+    ap.add_argument("--min-timed-ms", type=float, default=50.0, help="replay the K-step graph for at least this long")
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
     ap.add_argument("--reference-budget-s", type=float, default=90.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

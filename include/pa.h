@@ -361,6 +361,30 @@ PA_API pa_status pa_step(const pa_step_desc* step, void* stream);
  */
 PA_API pa_status pa_get_device_errors(uint32_t* errors, int32_t clear);
 
+/*
+ * pa_debug_set_wait_drill: a test hook for the kernels' bounded waits; the source pages have
+ * no counterpart. Every pipeline wait in the tensor-core kernels gives up after a time limit
+ * (1 s), raises PA_DEVERR_WAIT_TIMEOUT, lets the copies it already issued land, frees its
+ * tensor memory and returns without writing its results. The drill makes one such wait run
+ * out on purpose, with nothing in flight that the kernel abandons:
+ *   PA_DRILL_OFF              normal operation (limit back to 1 s; limit_ns is ignored)
+ *   PA_DRILL_DECODE_STAGE     bf16 grouped decode (pa_decode, pa_decode_append, pa_step):
+ *                             the warp that holds the first page of the work list announces
+ *                             16 bytes more on its first ring stage than its copies bring
+ *   PA_DRILL_PREFILL_K_TILE   tensor-core prefill (pa_prefill_chunk, pa_step): the CTA of the
+ *                             first Q-tile pair of kv head 0 of the longest sequence announces
+ *                             16 bytes more on its first K tile
+ * While a drill is on, limit_ns (1000 .. 10^9) is the wait limit of those kernels. The setting
+ * is process-wide and is read when a kernel is launched (a captured graph keeps the values of
+ * its capture). After a drilled call the results of that call are invalid and the decode
+ * workspace must be zero-filled again before its next use. Returns PA_ERR_INVALID_ARG for an
+ * unknown kind or a limit out of range, else PA_OK.
+ */
+#define PA_DRILL_OFF 0
+#define PA_DRILL_DECODE_STAGE 1
+#define PA_DRILL_PREFILL_K_TILE 2
+PA_API pa_status pa_debug_set_wait_drill(int32_t kind, uint64_t limit_ns);
+
 /* pa_status_string: static, human-readable name of a status code. */
 PA_API const char* pa_status_string(pa_status status);
 

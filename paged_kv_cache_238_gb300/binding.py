@@ -19,6 +19,7 @@ PA_DEVERR_SLOT_RANGE, PA_DEVERR_BLOCK_RANGE, PA_DEVERR_LEN_RANGE, PA_DEVERR_WAIT
 PA_DEVERR_APPEND_SLOT = 0x10
 PA_DECODE_TABLES_READY = 0x1
 PA_DECODE_POOL_READY = 0x2
+PA_DRILL_OFF, PA_DRILL_DECODE_STAGE, PA_DRILL_PREFILL_K_TILE = 0, 1, 2
 BLOCK_SIZE = 16
 
 #: every symbol that include/pa.h declares
@@ -29,7 +30,7 @@ EXPORTED = ("pa_reshape_and_cache", "pa_decode_workspace_size", "pa_decode", "pa
             "pa_bm_take_copies", "pa_bm_free_queue", "pa_bm_block_info", "pa_bm_num_blocks_for_memory", "pa_sha256",
             "pa_copy_blocks", "pa_reshape_and_cache_bs", "pa_decode_bs", "pa_prefill_chunk_bs",
             "pa_copy_blocks_bs", "pa_step", "pa_decode_append", "pa_bm_create_bs",
-            "pa_bm_num_blocks_for_memory_bs")
+            "pa_bm_num_blocks_for_memory_bs", "pa_debug_set_wait_drill")
 #: block sizes the *_bs entry points accept
 BLOCK_SIZES = (16, 32, 64, 128)
 #: size of the library's fixed scratch used by pa_decode_noalloc
@@ -92,6 +93,8 @@ def load(build_if_needed: bool = True) -> ctypes.CDLL:
                                               ctypes.c_int, vp]
             lib.pa_get_device_errors.restype = ctypes.c_int
             lib.pa_get_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
+            lib.pa_debug_set_wait_drill.restype = ctypes.c_int
+            lib.pa_debug_set_wait_drill.argtypes = [i32, ctypes.c_uint64]
             i64, pi32, pi64, pu8 = (ctypes.c_int64, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64),
                                     ctypes.POINTER(ctypes.c_uint8))
             for name, res, args in (
@@ -292,6 +295,12 @@ def pa_get_device_errors(clear: bool = True) -> int:
     v = ctypes.c_uint32(0)
     _check("pa_get_device_errors", load().pa_get_device_errors(ctypes.byref(v), 1 if clear else 0))
     return int(v.value)
+
+
+def pa_debug_set_wait_drill(kind: int, limit_ns: int = 0) -> None:
+    """Test hook: make one bounded wait of the named kernel run out (PA_DRILL_*), with
+    limit_ns as those kernels' wait limit; PA_DRILL_OFF restores normal operation."""
+    _check("pa_debug_set_wait_drill", load().pa_debug_set_wait_drill(int(kind), int(limit_ns)))
 
 
 def pa_prefill_chunk_bs(out, q, k_cache, v_cache, block_table, seq_lens, query_start_loc, max_chunk_len: int,

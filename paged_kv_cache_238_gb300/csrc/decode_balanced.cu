@@ -176,10 +176,10 @@ __device__ __forceinline__ void bulk_copy_g2s(void* smem_dst, const void* src, u
 }
 
 // Bounded wait that does not give up early on the abort flag (used to drain in-flight copies).
-__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
     const uint64_t t0 = global_timer_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (global_timer_ns() - t0 > kWaitLimitNs) return;
+        if (global_timer_ns() - t0 > limit_ns) return;
     }
 }
 
@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
     int32_t num_blocks, int32_t sub_log2, float scale_log2, int32_t nst, uint32_t stage_bytes, BalWorkspace ws,
     uint32_t* err, const int4* __restrict__ k_new, const int4* __restrict__ v_new,
     const int64_t* __restrict__ slot_mapping, int4* __restrict__ k_pool, int4* __restrict__ v_pool,
-    int32_t tables_ready, int32_t pool_ready) {
+    int32_t tables_ready, int32_t pool_ready, uint64_t wait_limit_ns, int32_t drill) {
     constexpr uint32_t kPage = kPageTokens * D * 2;
     constexpr uint32_t kHalves = D / 64;
     constexpr int KS = D / 16;  // k-steps over head_dim
@@ -456,10 +456,13 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
         };
         // Bytes that arrive in a stage besides the K and V pages: the segment's query rows with
         // its first page, the new token's rows with the page that holds position len - 1.
+        // With the wait drill on, the warp holding unit 0 announces 16 bytes more for its first
+        // stage than any copy brings: that stage never completes and its wait runs out.
+        const uint32_t drill_bytes = (drill && a_w == 0) ? 16u : 0u;
         auto extra_bytes = [&](int32_t t, const Walker& w) -> uint32_t {
             const bool seg_first = (t == 0) || (w.j == 0);
             const bool new_row = append && w.j == w.np - 1;
-            return (seg_first ? qbytes : 0u) + (new_row ? 4u * D : 0u);
+            return (seg_first ? qbytes : 0u) + (new_row ? 4u * D : 0u) + (t == 0 ? drill_bytes : 0u);
         };
         // The page copies of unit t (lane 0). With `arrive` the stage's single arrival is made
         // here together with every byte it expects; without it only the pages' bytes are
@@ -549,7 +552,8 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
 
         for (int32_t t = 0; t < n; ++t) {
             const int32_t st = t % nst;
-            const bool landed = mbar_wait_bounded(&bars[st], static_cast<uint32_t>(t / nst) & 1u, abort_flag);
+            const bool landed =
+                mbar_wait_bounded(&bars[st], static_cast<uint32_t>(t / nst) & 1u, abort_flag, wait_limit_ns);
             if (!__all_sync(0xffffffffu, landed)) {  // lanes agree before any warp-wide step
                 if (lane == 0) {
                     if (!*abort_flag) raise_error(err, PA_DEVERR_WAIT_TIMEOUT);
@@ -762,7 +766,8 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
         PA_TRACE_AT(g_trace, 12, static_cast<uint64_t>(n));
         // after an abort: let the copies already issued land before the CTA can exit
         if (consumed < issued && lane == 0) {
-            for (int32_t u = consumed; u < issued; ++u) mbar_drain(&bars[u % nst], static_cast<uint32_t>(u / nst) & 1u);
+            for (int32_t u = consumed; u < issued; ++u)
+                mbar_drain(&bars[u % nst], static_cast<uint32_t>(u / nst) & 1u, wait_limit_ns);
         }
     }
     if (tables_ready && n <= 0) dep_wait();  // warps without pages still merge and write
@@ -952,6 +957,7 @@ cudaError_t launch_impl(const DecodeArgs& a, const DecodePlan& plan, cudaStream_
                              static_cast<int>(plan.smem_bytes));
     if (e != cudaSuccess) return e;
     BalWorkspace ws = bal_ws(a.workspace, a.num_seqs, a.num_kv_heads, G, D, plan.num_ctas);
+    const WaitDrill drill = wait_drill();
 
     // Programmatic launch: the grid may be scheduled while the previous kernel in the stream
     // drains; it waits for that kernel (griddepcontrol.wait) before reading any input.
@@ -972,7 +978,7 @@ cudaError_t launch_impl(const DecodeArgs& a, const DecodePlan& plan, cudaStream_
                               a.err, static_cast<const int4*>(a.k_new), static_cast<const int4*>(a.v_new),
                               a.slot_mapping, static_cast<int4*>(const_cast<void*>(a.k_cache)),
                               static_cast<int4*>(const_cast<void*>(a.v_cache)), a.tables_ready ? 1 : 0,
-                              a.pool_ready ? 1 : 0);
+                              a.pool_ready ? 1 : 0, drill.limit_ns, drill.kind == kDrillDecodeStage ? 1 : 0);
 }
 
 // CTAs of the NW-warp kernel that fit on one SM with `smem` bytes of dynamic shared memory

@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "pa_internal.h"
@@ -230,7 +231,17 @@ pa_status prepare_prefill(void* out, const void* q, const void* k_cache, const v
 
 bool prefill_has_work(const PrefillArgs& a) { return a.num_seqs > 0 && a.max_chunk_len > 0; }
 
+std::atomic<int32_t> g_drill_kind{kDrillOff};
+std::atomic<uint64_t> g_drill_limit{kWaitLimitNs};
+
 }  // namespace
+
+WaitDrill wait_drill() {
+    WaitDrill d;
+    d.kind = g_drill_kind.load(std::memory_order_relaxed);
+    d.limit_ns = d.kind == kDrillOff ? kWaitLimitNs : g_drill_limit.load(std::memory_order_relaxed);
+    return d;
+}
 
 }  // namespace pa
 
@@ -481,6 +492,19 @@ PA_API pa_status pa_step(const pa_step_desc* d, void* stream_ptr) {
     // Join: later work on `stream` waits for the prefill too.
     if (cudaEventRecord(dev->join, dev->side) != cudaSuccess) return PA_ERR_CUDA;
     if (cudaStreamWaitEvent(s, dev->join, 0) != cudaSuccess) return PA_ERR_CUDA;
+    return PA_OK;
+}
+
+PA_API pa_status pa_debug_set_wait_drill(int32_t kind, uint64_t limit_ns) {
+    if (kind == PA_DRILL_OFF) {
+        g_drill_kind.store(kDrillOff);
+        g_drill_limit.store(kWaitLimitNs);
+        return PA_OK;
+    }
+    if (kind != PA_DRILL_DECODE_STAGE && kind != PA_DRILL_PREFILL_K_TILE) return PA_ERR_INVALID_ARG;
+    if (limit_ns < 1000 || limit_ns > kWaitLimitNs) return PA_ERR_INVALID_ARG;
+    g_drill_limit.store(limit_ns);
+    g_drill_kind.store(kind == PA_DRILL_DECODE_STAGE ? kDrillDecodeStage : kDrillPrefillKTile);
     return PA_OK;
 }
 

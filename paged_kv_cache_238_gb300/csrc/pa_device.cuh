@@ -42,10 +42,6 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
-// A pipeline wait gives up after this long; the kernel then raises PA_DEVERR_WAIT_TIMEOUT,
-// stops issuing copies and runs to completion without writing results.
-constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
-
 // ------------------------------------------------------------------------------------------
 // mbarrier
 // ------------------------------------------------------------------------------------------
@@ -91,23 +87,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Wait for the phase with the given parity to complete. Returns false when the wait gave up
 // (time limit) or when *abort is already set; never spins forever.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
         if (*abort) return false;
         if (mbar_try_wait(bar, parity)) return true;
-        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+        if (global_timer_ns() - t0 > limit_ns) return false;
     }
 }
 
 // Bounded wait that ignores the abort flag: used while winding down, to let copies or MMAs
 // already in flight complete before their shared or tensor memory is released. Returns
 // whether the phase completed in time.
-__device__ __forceinline__ bool mbar_wait_timeout(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_timeout(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
     const uint64_t t0 = global_timer_ns();
     while (!mbar_try_wait(bar, parity)) {
-        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+        if (global_timer_ns() - t0 > limit_ns) return false;
     }
     return true;
 }

@@ -74,6 +74,20 @@ struct DecodeArgs {
     bool pool_ready = false;
 };
 
+// A pipeline wait gives up after this long; the kernel then raises PA_DEVERR_WAIT_TIMEOUT,
+// stops issuing copies and runs to completion without writing results.
+constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
+
+// Wait drill (a test hook): with kind != kDrillOff the named kernel announces more bytes on one
+// barrier phase than any copy brings, so that one bounded wait runs out; limit_ns then replaces
+// the kernels' wait limit. Set through pa_debug_set_wait_drill; read by the launchers.
+enum WaitDrillKind : int32_t { kDrillOff = 0, kDrillDecodeStage = 1, kDrillPrefillKTile = 2 };
+struct WaitDrill {
+    int32_t kind;
+    uint64_t limit_ns;
+};
+WaitDrill wait_drill();
+
 enum DecodePath : int {
     kDecodeSimtSplit = 0,   // CUDA-core kernel over (sequence, kv head, partition) + reduce
     kDecodeMmaBalanced = 1  // persistent TMA + mma.sync kernel over a balanced page list + reduce

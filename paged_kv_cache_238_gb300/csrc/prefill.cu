@@ -64,8 +64,9 @@ struct TcSmem {
     static constexpr uint32_t total = misc + 16 + 1024;
 };
 
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* err) {
-    if (mbar_wait_bounded(bar, parity, abort)) return true;
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t* err,
+                                              uint64_t limit_ns) {
+    if (mbar_wait_bounded(bar, parity, abort, limit_ns)) return true;
     if (!*abort) raise_error(err, PA_DEVERR_WAIT_TIMEOUT);
     *abort = 1;
     return false;
@@ -106,7 +107,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
     __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ block_table,
     int32_t max_blocks, const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ query_start_loc,
-    int32_t num_kv_heads, int32_t num_blocks, int32_t sub_log2, float scale_log2, uint32_t* err) {
+    int32_t num_kv_heads, int32_t num_blocks, int32_t sub_log2, float scale_log2, uint32_t* err, uint64_t wait_limit_ns,
+    int32_t drill) {
     constexpr int TT = kTcRows / G;  // chunk tokens per Q tile
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -242,6 +244,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
         };
         int32_t win = 0;
         int32_t row_cur = page_row(lane), row_nxt = page_row(32 + lane);
+        // With the wait drill on, one CTA's K producer announces 16 bytes more for its first
+        // tile than the copies bring: that tile never completes and the MMA warp's wait runs out.
+        const uint32_t drill_bytes = (drill && warp == kKWarp && pair == 0 && h == 0 && blockIdx.z == 0) ? 16u : 0u;
         for (int32_t j = 0; j < n_kv; ++j) {
             const int32_t st = j % nst;
             const uint32_t use = static_cast<uint32_t>(j / nst);
@@ -252,11 +257,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
             }
             // tile j's stage is free once the MMAs of tile j - nst that read it are done
             bool ok = true;
-            if (use > 0 && lane == 0) ok = wait_or_abort(&empty[st], (use - 1) & 1u, abort_flag, err);
+            if (use > 0 && lane == 0) ok = wait_or_abort(&empty[st], (use - 1) & 1u, abort_flag, err, wait_limit_ns);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             uint8_t* dst = ring + st * kTile;
-            if (lane == 0) mbar_arrive_expect_tx(&full[st], kTile);
+            if (lane == 0) mbar_arrive_expect_tx(&full[st], kTile + (j == 0 ? drill_bytes : 0u));
             last_j = j;
             const int32_t rk = __shfl_sync(0xffffffffu, row_cur, (j & 3) * 8 + (lane & 7));
             __syncwarp();
@@ -306,11 +311,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
         };
         auto wait_k = [&](int32_t j) {
             const bool ok = wait_or_abort(&k_full[j % kKStages], static_cast<uint32_t>(j / kKStages) & 1u,
-                                          abort_flag, err);
+                                          abort_flag, err, wait_limit_ns);
             umma::fence_after_sync();
             return ok;
         };
-        bool ok = wait_or_abort(q_full, 0, abort_flag, err) && wait_k(0);
+        bool ok = wait_or_abort(q_full, 0, abort_flag, err, wait_limit_ns) && wait_k(0);
         if (ok) {
             qk(0, 0);
             if (active_b) qk(1, 0);
@@ -319,9 +324,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
         for (int32_t j = 0; j < n_kv && ok; ++j) {
             const bool ua = j < n_kv_a, ub = j < n_kv_b;
             const bool ua1 = j + 1 < n_kv_a, ub1 = j + 1 < n_kv_b;
-            ok = wait_or_abort(&v_full[j % kVStages], static_cast<uint32_t>(j / kVStages) & 1u, abort_flag, err);
+            ok = wait_or_abort(&v_full[j % kVStages], static_cast<uint32_t>(j / kVStages) & 1u, abort_flag, err, wait_limit_ns);
             if (ok && ua) {
-                ok = wait_or_abort(&p_full[0], j & 1, abort_flag, err);  // P_a(j) written, S_a(j) read
+                ok = wait_or_abort(&p_full[0], j & 1, abort_flag, err, wait_limit_ns);  // P_a(j) written, S_a(j) read
                 umma::fence_after_sync();
                 if (ok) pv(0, j);
                 if (ok && !ua1 && leader) umma::commit(&o_done[0]);
@@ -329,7 +334,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
             if (ok && (ua1 || ub1)) ok = wait_k(j + 1);
             if (ok && ua1) qk(0, j + 1);
             if (ok && ub) {
-                ok = wait_or_abort(&p_full[1], j & 1, abort_flag, err);
+                ok = wait_or_abort(&p_full[1], j & 1, abort_flag, err, wait_limit_ns);
                 umma::fence_after_sync();
                 if (ok) pv(1, j);
                 if (ok && !ub1 && leader) umma::commit(&o_done[1]);
@@ -354,7 +359,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
         float m_ref = -INFINITY, l_sum = 0.f;
         bool ok = true;
         for (int32_t j = 0; j < n_kv_x; ++j) {
-            ok = wait_or_abort(&s_full[xq], j & 1, abort_flag, err);
+            ok = wait_or_abort(&s_full[xq], j & 1, abort_flag, err, wait_limit_ns);
             if (!__all_sync(0xffffffffu, ok)) {
                 ok = false;
                 break;
@@ -445,7 +450,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
             // by the first Q tile that uses key tile j
             if ((xq == 0 || j >= n_kv_a) && kbase + r >= L) {
                 const int32_t st = j % kVStages;
-                const bool okv = wait_or_abort(&v_full[st], static_cast<uint32_t>(j / kVStages) & 1u, abort_flag, err);
+                const bool okv = wait_or_abort(&v_full[st], static_cast<uint32_t>(j / kVStages) & 1u, abort_flag, err, wait_limit_ns);
                 if (okv) {
                     uint8_t* sv_tile = smem + TcSmem::v + st * kTile;
 #pragma unroll
@@ -461,7 +466,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
             if (lane == 0) mbar_arrive(&p_full[xq]);
         }
         if (ok && n_kv_x > 0) {
-            ok = wait_or_abort(&o_done[xq], 0, abort_flag, err);
+            ok = wait_or_abort(&o_done[xq], 0, abort_flag, err, wait_limit_ns);
             ok = __all_sync(0xffffffffu, ok);
         }
         if (ok && n_kv_x > 0) {
@@ -493,9 +498,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
         const int32_t nst = warp == kVWarp ? kVStages : kKStages;
         uint64_t* full = warp == kVWarp ? v_full : k_full;
         for (int32_t j = max(0, last_j - nst + 1); j <= last_j; ++j)
-            mbar_wait_timeout(&full[j % nst], static_cast<uint32_t>(j / nst) & 1u);
+            mbar_wait_timeout(&full[j % nst], static_cast<uint32_t>(j / nst) & 1u, wait_limit_ns);
     }
-    if (warp == kMmaWarp && lane == 0) mbar_wait_timeout(idle, 0);  // any thread may wait on the barrier
+    if (warp == kMmaWarp && lane == 0) mbar_wait_timeout(idle, 0, wait_limit_ns);  // any thread may wait on the barrier
     umma::fence_before_sync();
     __syncthreads();
     if (warp == kMmaWarp) {
@@ -519,10 +524,12 @@ cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t stream) {
     const int32_t tiles = (a.max_chunk_len + TT - 1) / TT;
     const int32_t pairs = (tiles + 1) / 2;
     dim3 grid(pairs, a.num_kv_heads, a.num_seqs);
+    const WaitDrill drill = wait_drill();
     prefill_tc_kernel<G><<<grid, kTcThreads, TcSmem::total, stream>>>(
         tm_k, tm_v, static_cast<__nv_bfloat16*>(a.out), static_cast<const __nv_bfloat16*>(a.q), a.block_table,
         a.max_blocks_per_seq, a.seq_lens, a.query_start_loc, a.num_kv_heads, a.num_blocks,
-        block_size_log2(a.block_size) - 4, a.scale * kLog2e, a.err);
+        block_size_log2(a.block_size) - 4, a.scale * kLog2e, a.err, drill.limit_ns,
+        drill.kind == kDrillPrefillKTile ? 1 : 0);
     return cudaGetLastError();
 }
 

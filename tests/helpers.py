@@ -9,6 +9,8 @@ Tolerances (written here once, used by every parity test):
 """
 from __future__ import annotations
 
+import functools
+
 import numpy as np
 
 from paged_kv_cache_238_gb300 import workloads as W
@@ -85,3 +87,19 @@ class DeviceWorkload:
         if self.wl.slot_mapping is not None:
             oracle.reshape_and_cache(self.wl.k_new, self.wl.v_new, kc, vc, self.wl.slot_mapping)
         return kc, vc
+
+
+@functools.lru_cache(maxsize=1)
+def mixed_step_reference():
+    """Oracle results for the whole mixed-step workload, computed once per test session:
+    (pool K, pool V after the step's slot writes, every decode row's output, every prefill
+    row's output). Both attentions see the pool after all of the step's writes, as the step
+    runs them (the writes come first)."""
+    import oracle
+    wl = W.mixed_step()
+    kc, vc = wl.k_cache.copy(), wl.v_cache.copy()
+    oracle.reshape_and_cache(wl.k_new, wl.v_new, kc, vc, wl.slot_mapping)
+    ref_dec = oracle.attention(wl.q, kc, vc, wl.block_table, wl.seq_lens, wl.scale)
+    ref_pre = oracle.attention(wl.q_prefill, kc, vc, wl.block_table_prefill, wl.seq_lens_prefill, wl.scale,
+                               query_start_loc=wl.query_start_loc)
+    return wl, kc, vc, ref_dec, ref_pre

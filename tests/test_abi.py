@@ -239,3 +239,19 @@ def test_decode_append_rejects_bad_arguments(kw, expect):
     assert B.load().pa_decode_append(a["out"], a["q"], a["k_new"], a["v_new"], a["slots"], a["kc"], a["vc"], a["bt"],
                                      a["mb"], a["lens"], a["S"], a["max_len"], a["Hq"], a["Hkv"], a["D"], a["NB"],
                                      a["bs"], 0.1, a["dt"], FAKE, 1 << 24, a.get("flags", 0), None) == expect
+
+
+def test_wait_drill_arguments_are_checked_on_the_host():
+    """The wait-drill hook only sets host-side state: unknown kinds and limits outside
+    1 us .. 1 s are rejected, valid settings are taken and PA_DRILL_OFF restores normal
+    operation (no kernel runs here)."""
+    lib = B.load()
+    assert lib.pa_debug_set_wait_drill(3, 2_000_000) == B.PA_ERR_INVALID_ARG
+    assert lib.pa_debug_set_wait_drill(-1, 2_000_000) == B.PA_ERR_INVALID_ARG
+    assert lib.pa_debug_set_wait_drill(B.PA_DRILL_DECODE_STAGE, 999) == B.PA_ERR_INVALID_ARG
+    assert lib.pa_debug_set_wait_drill(B.PA_DRILL_DECODE_STAGE, 1_000_000_001) == B.PA_ERR_INVALID_ARG
+    try:
+        assert lib.pa_debug_set_wait_drill(B.PA_DRILL_DECODE_STAGE, 2_000_000) == B.PA_OK
+        assert lib.pa_debug_set_wait_drill(B.PA_DRILL_PREFILL_K_TILE, 1000) == B.PA_OK
+    finally:
+        assert lib.pa_debug_set_wait_drill(B.PA_DRILL_OFF, 0) == B.PA_OK

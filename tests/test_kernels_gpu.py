@@ -14,7 +14,7 @@ import oracle  # noqa: E402
 from paged_kv_cache_238_gb300 import binding as B  # noqa: E402
 from paged_kv_cache_238_gb300 import workloads as W  # noqa: E402
 
-from helpers import DeviceWorkload, assert_close, to_f64, to_host_bits  # noqa: E402
+from helpers import DeviceWorkload, assert_close, mixed_step_reference, to_f64, to_host_bits  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 
@@ -111,11 +111,14 @@ def test_decode_long_split_kv():
 
 
 @pytest.mark.slow
-def test_mixed_step_decode_rows_sampled():
-    wl = W.mixed_step()
-    rng = np.random.default_rng(7)
-    rows = np.sort(rng.choice(wl.S, size=48, replace=False))
-    _decode_vs_oracle(wl, rows=rows, what="mixed step, decode rows")
+def test_mixed_step_decode_all_rows():
+    """All 240 decode rows of the mixed-step workload, element by element."""
+    wl, kc, vc, ref_dec, _ = mixed_step_reference()
+    dw = DeviceWorkload(wl)
+    run_reshape(dw)
+    out = run_decode(dw)
+    check_pool(dw, kc, vc)
+    assert_close(out, ref_dec, "bf16", "mixed step, every decode row")
 
 
 # ----------------------------------------------------------------------------- decode: edge cases
@@ -275,36 +278,17 @@ def test_prefill_empty_chunks_and_whole_prompt():
     assert_close(out, ref, "bf16", "empty chunks")
 
 
-def _sampled_prefill_rows(wl, rng, per_seq=6):
-    """(row, seq, visible length) for sampled chunk rows: row r of a chunk sits at position
-    L - C + r, so it equals a decode query of length L - C + r + 1 on the same table row."""
-    qsl = wl.query_start_loc
-    out = []
-    for i in range(len(qsl) - 1):
-        C = int(qsl[i + 1] - qsl[i])
-        if C == 0:
-            continue
-        L = int(wl.seq_lens_prefill[i])
-        rs = set(rng.choice(C, size=min(per_seq, C), replace=False).tolist()) | {0, C - 1}
-        out += [(int(qsl[i]) + r, i, L - C + r + 1) for r in sorted(rs)]
-    return out
-
-
 @pytest.mark.slow
-def test_mixed_step_prefill_rows_sampled():
-    wl = W.mixed_step()
+def test_mixed_step_prefill_all_rows():
+    """Every row of all 16 prefill chunks of the mixed-step workload (8192 query rows over
+    prior contexts of 0..4096 tokens), element by element, and the pool after the step's
+    writes bit-exact."""
+    wl, kc, vc, _, ref_pre = mixed_step_reference()
     dw = DeviceWorkload(wl)
     run_reshape(dw)
     out = run_prefill(dw)
-    kc, vc = dw.host_pool_after_writes()
-    picks = _sampled_prefill_rows(wl, np.random.default_rng(8))
-    rows = np.array([p[0] for p in picks])
-    seqs = np.array([p[1] for p in picks])
-    lens = np.array([p[2] for p in picks], np.int32)
-    ref = oracle.attention(wl.q_prefill[rows], kc, vc, wl.block_table_prefill[seqs], lens, wl.scale)
-    assert_close(out[rows], ref, "bf16", "mixed step, prefill rows")
-    # the pool after the step's writes is bit-exact too
     check_pool(dw, kc, vc)
+    assert_close(out, ref_pre, "bf16", "mixed step, every prefill row")
 
 
 # ----------------------------------------------------------------------------- maximum sizes
