@@ -33,7 +33,9 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "pa_oracle.c")
-_LIB = os.path.join(_HERE, "liboracle.so")
+# PA_SANITIZE=address,undefined: a sanitizer build (liboracle_san.so), as for libpa
+_SANITIZE = os.environ.get("PA_SANITIZE", "").strip()
+_LIB = os.path.join(_HERE, "liboracle_san.so" if _SANITIZE else "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
@@ -48,7 +50,8 @@ def build(force: bool = False) -> str:
             and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
         return _LIB
     tmp = _LIB + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
+    san = [f"-fsanitize={_SANITIZE}", "-fno-omit-frame-pointer", "-g"] if _SANITIZE else []
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared"] + san + [_SRC, "-o", tmp, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB)
     return _LIB

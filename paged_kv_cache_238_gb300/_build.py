@@ -17,12 +17,24 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
-LIB = os.path.join(HERE, "libpa.so")
+# PA_SANITIZE=address,undefined (any -fsanitize list) builds the host code with gcc's
+# sanitizers into libpa_san.so instead, under _build_san/; run the process with the sanitizer
+# runtimes preloaded (LD_PRELOAD of libasan.so and libubsan.so).
+SANITIZE = os.environ.get("PA_SANITIZE", "").strip()
+if SANITIZE:
+    BUILD = os.path.join(HERE, "_build_san")
+    LIB = os.path.join(HERE, "libpa_san.so")
+else:
+    LIB = os.path.join(HERE, "libpa.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
+# (nvcc's -Xcompiler splits at commas: one -fsanitize= per sanitizer)
+_SAN = ",".join(f"-fsanitize={x.strip()}" for x in SANITIZE.split(",") if x.strip())
+_HOST = "-fPIC,-fvisibility=hidden" + (f",{_SAN},-fno-omit-frame-pointer,-g" if SANITIZE else "")
+NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", _HOST,
                      "--expt-relaxed-constexpr", "-I", INCLUDE]
-LINK_FLAGS = ARCH + ["-shared", "-Xlinker", "--exclude-libs,ALL", "-Xlinker", "-Bsymbolic"]
+LINK_FLAGS = ARCH + ["-shared", "-Xlinker", "--exclude-libs,ALL", "-Xlinker", "-Bsymbolic"] + (
+    ["-Xcompiler", _SAN] if SANITIZE else [])
 
 
 def nvcc_path() -> str:
