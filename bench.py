@@ -86,9 +86,11 @@ def _kv_token_bytes(wl) -> int:
 
 
 def step_bytes(wl) -> dict:
-    """Algorithmic bytes of one step: every visible key's K and V once, Q and output, the
+    """Algorithmic bytes of one step: every distinct visible key's K and V once (a prefix that
+    several sequences alias counts once: it need leave HBM only once), Q and output, the
     block-table entries a kernel must read, lengths, and the new tokens' K/V read and written
-    (plus their slots). Prefill flops count visible (query, key) pairs only."""
+    (plus their slots). Prefill flops count visible (query, key) pairs only. "decode_logical"
+    counts each sequence's keys instead."""
     el = 2 if wl.dtype == "bf16" else 4
     tok = _kv_token_bytes(wl)
     res = {"decode": 0, "prefill": 0, "reshape": 0, "kv": 0, "prefill_flops": 0, "kv_unique": 0}
@@ -97,7 +99,6 @@ def step_bytes(wl) -> dict:
         kv = int(lens.sum()) * tok
         q = wl.S * wl.H_q * wl.D * el
         bt = int(np.sum(-(-lens // 16))) * 4
-        res["decode"] = kv + 2 * q + bt + wl.S * 4
         res["kv"] += kv
         # distinct (block, row) pairs actually holding visible keys: aliased prefixes count once
         seen = {}
@@ -106,7 +107,10 @@ def step_bytes(wl) -> dict:
             for j in range(-(-n // 16)):
                 b = int(wl.block_table[i, j])
                 seen[b] = max(seen.get(b, 0), min(16, n - 16 * j))
-        res["kv_unique"] += sum(seen.values()) * tok
+        kv_u = sum(seen.values()) * tok
+        res["kv_unique"] += kv_u
+        res["decode"] = kv_u + 2 * q + bt + wl.S * 4
+        res["decode_logical"] = kv + 2 * q + bt + wl.S * 4
     if wl.seq_lens_prefill is not None:
         L = wl.seq_lens_prefill.astype(np.int64)
         C = np.diff(wl.query_start_loc).astype(np.int64)
@@ -818,12 +822,12 @@ def run_ours(args):
         line["config"]["decode_bytes_per_call"] = nbytes["decode"]
         line["config"]["mean_len"] = round(float(wl.seq_lens.mean()), 2)
     if nbytes["kv_unique"] < nbytes["kv"]:
-        # aliased prefix blocks: the logical bytes count each sequence's keys; DRAM sees the
-        # distinct blocks once (the rest is served from L2)
+        # aliased prefix blocks: value and roofline count the distinct keys (what must leave
+        # HBM); the logical figure counts each sequence's keys and is context only
         line["config"]["kv_bytes_logical"] = nbytes["kv"]
         line["config"]["kv_bytes_distinct"] = nbytes["kv_unique"]
-        line["decode_distinct_hbm_frac"] = round(
-            (nbytes["decode"] - nbytes["kv"] + nbytes["kv_unique"]) / (kern_ms["decode"] * 1e-3) / 1e9 / hbm_peak, 4)
+        line["config"]["bytes_basis"] = "distinct keys (an aliased prefix counts once)"
+        line["decode_logical_tbs"] = round(nbytes["decode_logical"] / (kern_ms["decode"] * 1e-3) / 1e12, 3)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_budget_s,
                                             {"tokens/s": "tokens", "TFLOP/s": "flops"}.get(unit, "step"))
