@@ -392,7 +392,7 @@ class DeviceStep:
     reshape_and_cache of the step's new tokens, then chunked prefill and decode attention."""
 
     def __init__(self, wl, dev, R: int, stream, whole_step: bool = False, decode_sms: int = 0,
-                 fuse_append: bool = False, pool_ready: bool = False):
+                 fuse_append: bool = False, pool_ready: bool = False, shared_prefix: bool = False):
         import torch
         from paged_kv_cache_238_gb300 import binding as B
         self.B, self.wl, self.stream, self.R = B, wl, stream, R
@@ -414,8 +414,14 @@ class DeviceStep:
             self.out = torch.empty_like(self.q)
             self.msl = int(wl.seq_lens.max())
             dt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
-            self.ws = torch.zeros(max(16, B.pa_decode_workspace_size(wl.S, wl.H_q, wl.H_kv, wl.D, self.msl, dt)),
-                                  dtype=torch.uint8, device=dev)
+            # a prefix that every sequence aliases: attended once (pa_decode_shared_prefix)
+            self.prefix = int(wl.info.get("shared_prefix_tokens", 0)) if shared_prefix else 0
+            if self.prefix:
+                n = B.pa_decode_shared_prefix_workspace_size(wl.S, wl.H_q, wl.H_kv, wl.D, self.msl, self.prefix)
+                if n == 0:
+                    self.prefix = 0
+            ws_bytes = n if self.prefix else B.pa_decode_workspace_size(wl.S, wl.H_q, wl.H_kv, wl.D, self.msl, dt)
+            self.ws = torch.zeros(max(16, ws_bytes), dtype=torch.uint8, device=dev)
             self.inputs += [self.q, self.bt, self.lens]
             self.outputs.append(self.out)
         if self.has_pre:
@@ -529,8 +535,12 @@ class DeviceStep:
             rec("prefill", 1)
         if self.has_dec:
             rec("decode", 0)
-            B.pa_decode(T["out"], T["q"], self.kcs[r], self.vcs[r], T["bt"], T["lens"], self.msl, wl.scale,
-                        self.ws, stream=s)
+            if self.prefix:
+                B.pa_decode_shared_prefix(T["out"], T["q"], self.kcs[r], self.vcs[r], T["bt"], T["lens"], self.msl,
+                                          wl.scale, self.prefix, self.ws, stream=s)
+            else:
+                B.pa_decode(T["out"], T["q"], self.kcs[r], self.vcs[r], T["bt"], T["lens"], self.msl, wl.scale,
+                            self.ws, stream=s)
             rec("decode", 1)
 
 
@@ -563,7 +573,8 @@ def run_ours(args):
     R = args.replicas
     stream = torch.cuda.Stream(device=dev)
     step = DeviceStep(wl, dev, R, stream, whole_step=not args.sequential, decode_sms=args.decode_sms,
-                      fuse_append=not args.sequential, pool_ready=not args.no_pool_ready)
+                      fuse_append=not args.sequential, pool_ready=not args.no_pool_ready,
+                      shared_prefix=not args.no_shared_prefix)
     if step.fused_append:
         # one kernel writes the new tokens and attends: its algorithmic bytes are the decode's
         # plus the new rows read once from the input and written once (not read back)
@@ -906,6 +917,8 @@ def main(argv=None):
     ap.add_argument("--sequential", action="store_true",
                     help="one call per kernel: no pa_step (mixed step) and no pa_decode_append (decode step)")
     ap.add_argument("--decode-sms", type=int, default=0, help="pa_step: SMs held by decode (0 = 27/64 of them)")
+    ap.add_argument("--no-shared-prefix", action="store_true",
+                    help="prefix_sharing: plain pa_decode instead of pa_decode_shared_prefix")
     ap.add_argument("--no-pool-ready", action="store_true",
                     help="decode step without PA_DECODE_POOL_READY (first page copies after the grid-dependency wait)")
     args = ap.parse_args(argv)

@@ -84,6 +84,8 @@ typedef enum {
 #define PA_DEVERR_WAIT_TIMEOUT 0x8u  /* a bounded pipeline wait gave up (results invalid) */
 #define PA_DEVERR_APPEND_SLOT  0x10u /* pa_decode_append: slot_mapping[i] is not the slot the
                                         block table gives position seq_lens[i] - 1          */
+#define PA_DEVERR_PREFIX_MISMATCH 0x20u /* pa_decode_shared_prefix: a table row does not start
+                                           with row 0's prefix blocks (results invalid)   */
 
 /*
  * pa_reshape_and_cache: write the K/V rows of num_tokens new tokens into their slots.
@@ -167,6 +169,41 @@ PA_API pa_status pa_decode(void* out, const void* q, const void* k_cache, const 
                     int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                     int32_t num_blocks, float scale, pa_dtype dtype,
                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * pa_decode_shared_prefix: pa_decode for a batch whose sequences all begin with the same
+ * prefix_tokens keys in the same physical blocks (the first prefix_tokens / 16 entries of every
+ * block-table row equal row 0's). Identical prefixes point at the same physical blocks
+ * ("vLLM Internals", section 1.2); this call also computes over them once instead of once per
+ * sequence. The result is pa_decode's (same arguments, bf16 only), up to rounding: softmax over
+ * a sequence's keys is split into the shared prefix and the sequence's own suffix, each reduced
+ * to (normalised output, max, sum), and the two are merged by the log-sum-exp rule.
+ *   - The suffix part is the balanced decode kernel over keys [prefix_tokens, seq_lens[i]),
+ *     on a grid capped to leave SMs for the prefix part, written as fp32 parts into the
+ *     workspace; it also checks the table: a row whose prefix entries differ from row 0's sets
+ *     PA_DEVERR_PREFIX_MISMATCH (the results are then invalid). The prefix part runs on the
+ *     tensor cores, all sequences' query rows of one kv head together against the prefix's key
+ *     tiles (no causal bound), as a programmatic dependent launch: it starts on the free SMs
+ *     while the decode streams, waits for the decode grid only at its end, merges each row's
+ *     suffix part and writes `out`. Both kernels launch on `stream`.
+ *   - prefix_tokens: a positive multiple of 16, at most max_seq_len; every seq_lens[i] must be
+ *     at least prefix_tokens (a shorter one sets PA_DEVERR_LEN_RANGE).
+ *   - Supported: bf16, head_dim 128, 4, 8 or 16 q heads per kv head, at most 1024 sequences
+ *     (PA_ERR_UNSUPPORTED otherwise).
+ *   - workspace: >= pa_decode_shared_prefix_workspace_size(...) bytes, 16-byte aligned,
+ *     zero-filled before its first use, under the rules of pa_decode_workspace_size (its first
+ *     part is the suffix decode's workspace).
+ * No counterpart entry point exists on the source pages; they describe the sharing of the
+ * blocks, and this computes on that sharing.
+ */
+PA_API size_t pa_decode_shared_prefix_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                                     int32_t head_dim, int32_t max_seq_len, int32_t prefix_tokens);
+PA_API pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                         const int32_t* block_table, int32_t max_blocks_per_seq,
+                                         const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                                         int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                         int32_t num_blocks, float scale, int32_t prefix_tokens, void* workspace,
+                                         size_t workspace_bytes, void* stream);
 
 /*
  * pa_decode_append: one decode step with its new tokens, in one launch where it can be. For

@@ -17,6 +17,7 @@ PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_NO_SPACE = 0,
 PA_F32, PA_BF16 = 0, 1
 PA_DEVERR_SLOT_RANGE, PA_DEVERR_BLOCK_RANGE, PA_DEVERR_LEN_RANGE, PA_DEVERR_WAIT_TIMEOUT = 0x1, 0x2, 0x4, 0x8
 PA_DEVERR_APPEND_SLOT = 0x10
+PA_DEVERR_PREFIX_MISMATCH = 0x20
 PA_DECODE_TABLES_READY = 0x1
 PA_DECODE_POOL_READY = 0x2
 PA_DRILL_OFF, PA_DRILL_DECODE_STAGE, PA_DRILL_PREFILL_K_TILE = 0, 1, 2
@@ -30,7 +31,8 @@ EXPORTED = ("pa_reshape_and_cache", "pa_decode_workspace_size", "pa_decode", "pa
             "pa_bm_take_copies", "pa_bm_free_queue", "pa_bm_block_info", "pa_bm_num_blocks_for_memory", "pa_sha256",
             "pa_copy_blocks", "pa_reshape_and_cache_bs", "pa_decode_bs", "pa_prefill_chunk_bs",
             "pa_copy_blocks_bs", "pa_step", "pa_decode_append", "pa_bm_create_bs",
-            "pa_bm_num_blocks_for_memory_bs", "pa_debug_set_wait_drill")
+            "pa_bm_num_blocks_for_memory_bs", "pa_debug_set_wait_drill", "pa_decode_shared_prefix_workspace_size",
+            "pa_decode_shared_prefix")
 #: block sizes the *_bs entry points accept
 BLOCK_SIZES = (16, 32, 64, 128)
 #: size of the library's fixed scratch used by pa_decode_noalloc
@@ -93,6 +95,11 @@ def load(build_if_needed: bool = True) -> ctypes.CDLL:
                                               ctypes.c_int, vp]
             lib.pa_get_device_errors.restype = ctypes.c_int
             lib.pa_get_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
+            lib.pa_decode_shared_prefix_workspace_size.restype = sz
+            lib.pa_decode_shared_prefix_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
+            lib.pa_decode_shared_prefix.restype = ctypes.c_int
+            lib.pa_decode_shared_prefix.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, f32, i32,
+                                                    vp, sz, vp]
             lib.pa_debug_set_wait_drill.restype = ctypes.c_int
             lib.pa_debug_set_wait_drill.argtypes = [i32, ctypes.c_uint64]
             i64, pi32, pi64, pu8 = (ctypes.c_int64, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64),
@@ -225,6 +232,26 @@ def pa_decode(out, q, k_cache, v_cache, block_table, seq_lens, max_seq_len: int,
     _check("pa_decode", lib.pa_decode(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
         _ptr(seq_lens), S, int(max_seq_len), H_q, H_kv, D, NB, float(scale), _dtype_code(q), _ptr(workspace),
+        ws_bytes, _stream(stream)))
+
+
+def pa_decode_shared_prefix_workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                                           max_seq_len: int, prefix_tokens: int) -> int:
+    return int(load().pa_decode_shared_prefix_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                             max_seq_len, prefix_tokens))
+
+
+def pa_decode_shared_prefix(out, q, k_cache, v_cache, block_table, seq_lens, max_seq_len: int, scale: float,
+                            prefix_tokens: int, workspace, stream=None) -> None:
+    """pa_decode for a batch whose table rows all start with the same prefix_tokens / 16 block
+    ids (C ABI pa_decode_shared_prefix): the prefix is attended once per kv head; bf16."""
+    _need_cuda(out, q, k_cache, v_cache, block_table, seq_lens, workspace)
+    S, H_q, D = q.shape
+    NB, H_kv = k_cache.shape[0], k_cache.shape[1]
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("pa_decode_shared_prefix", load().pa_decode_shared_prefix(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
+        _ptr(seq_lens), S, int(max_seq_len), H_q, H_kv, D, NB, float(scale), int(prefix_tokens), _ptr(workspace),
         ws_bytes, _stream(stream)))
 
 

@@ -191,7 +191,8 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity, uint6
 //   M' = max(M, m_j),  den = den 2^(M - M') + sum_j l_j 2^(m_j - M'),  acc likewise with o_j.
 template <int D>
 __device__ __forceinline__ void merge_pieces(__nv_bfloat16* o, int32_t a, int32_t w_first, int32_t w_last, int64_t U,
-                                             int64_t W, int32_t G, const BalWorkspace& ws, int32_t lane) {
+                                             int64_t W, int32_t G, const BalWorkspace& ws, int32_t lane,
+                                             const PartOut& part, int64_t row0) {
     constexpr int E = D / 32;
     const bool may_be_empty = U < W;
     const int32_t first_slot = slice_start(w_first, U, W) < a ? 1 : 0;
@@ -256,6 +257,13 @@ __device__ __forceinline__ void merge_pieces(__nv_bfloat16* o, int32_t a, int32_
         for (int k = 0; k < 4; ++k) {
             if (g0 + k < G) {
                 const float inv = 1.f / den[k];
+                if (part.o != nullptr) {  // a part: normalised fp32 row and its (max, sum)
+                    float* po = part.o + (row0 + g0 + k) * D + lane * E;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) po[e] = acc[k][e] * inv;
+                    if (lane == 0) part.ml[row0 + g0 + k] = make_float2(M[k], den[k]);
+                    continue;
+                }
                 uint32_t* dst = reinterpret_cast<uint32_t*>(o + (g0 + k) * D + lane * E);
                 dst[0] = pack_bf16x2(acc[k][0] * inv, acc[k][1] * inv);
                 if constexpr (E == 4) dst[1] = pack_bf16x2(acc[k][2] * inv, acc[k][3] * inv);
@@ -283,7 +291,8 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
     int32_t num_blocks, int32_t sub_log2, float scale_log2, int32_t nst, uint32_t stage_bytes, BalWorkspace ws,
     uint32_t* err, const int4* __restrict__ k_new, const int4* __restrict__ v_new,
     const int64_t* __restrict__ slot_mapping, int4* __restrict__ k_pool, int4* __restrict__ v_pool,
-    int32_t tables_ready, int32_t pool_ready, uint64_t wait_limit_ns, int32_t drill) {
+    int32_t tables_ready, int32_t pool_ready, uint64_t wait_limit_ns, int32_t drill, int32_t len_offset,
+    PartOut part) {
     constexpr uint32_t kPage = kPageTokens * D * 2;
     constexpr uint32_t kHalves = D / 64;
     constexpr int KS = D / 16;  // k-steps over head_dim
@@ -305,7 +314,9 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
     int32_t* lens = reinterpret_cast<int32_t*>(smem + L.lens);
 
     const int32_t tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int32_t cap = table_tokens(max_blocks, sub_log2);
+    // keys [len_offset, len) of each sequence; the caller's table row begins at its
+    // len_offset / block_size-th entry
+    const int32_t cap = table_tokens(max_blocks, sub_log2) - len_offset;
     const int32_t Hq = G * num_kv_heads;
     PA_TRACE_DECL
     PA_TRACE_BEGIN(g_trace_counter);
@@ -337,7 +348,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
         const int32_t b = min(S, tid * per), e = min(S, b + per);
         int32_t local = 0;
         for (int32_t s = b; s < e; ++s) {
-            int32_t len = __ldg(seq_lens + s);
+            int32_t len = __ldg(seq_lens + s) - len_offset;
             if (len < 0 || len > cap) {
                 if (blockIdx.x == 0) raise_error(err, PA_DEVERR_LEN_RANGE);
                 len = len < 0 ? 0 : cap;
@@ -373,6 +384,17 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
         __syncthreads();
     }
     PA_TRACE_STAMP(g_trace, 1);
+    if (len_offset > 0) {
+        // every table row must begin with row 0's prefix blocks (the caller's rows start
+        // len_offset / block_size entries before the ones this kernel walks)
+        const int32_t pb = len_offset >> (sub_log2 + 4);
+        const int32_t* bt0 = block_table - pb;
+        const int64_t n_ids = static_cast<int64_t>(S) * pb;
+        for (int64_t i = static_cast<int64_t>(blockIdx.x) * NTH + tid; i < n_ids; i += static_cast<int64_t>(gridDim.x) * NTH) {
+            const int64_t s = i / pb, j = i - s * pb;
+            if (__ldg(bt0 + s * max_blocks + j) != __ldg(bt0 + j)) raise_error(err, PA_DEVERR_PREFIX_MISMATCH);
+        }
+    }
 
     const int64_t U = prefix[S];
     const int64_t C = gridDim.x;
@@ -388,8 +410,13 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
     for (int32_t s = blockIdx.x; s < S; s += gridDim.x) {
         if (lens[s] != 0) continue;
         if (tables_ready) dep_wait();
-        uint32_t* z = reinterpret_cast<uint32_t*>(out + static_cast<int64_t>(s) * Hq * D);
-        for (int32_t i = tid; i < Hq * D / 2; i += NTH) z[i] = 0u;
+        if (part.o != nullptr) {  // an empty part: zero output, weight zero
+            for (int32_t i = tid; i < Hq * D; i += NTH) part.o[static_cast<int64_t>(s) * Hq * D + i] = 0.f;
+            for (int32_t i = tid; i < Hq; i += NTH) part.ml[static_cast<int64_t>(s) * Hq + i] = make_float2(-INFINITY, 0.f);
+        } else {
+            uint32_t* z = reinterpret_cast<uint32_t*>(out + static_cast<int64_t>(s) * Hq * D);
+            for (int32_t i = tid; i < Hq * D / 2; i += NTH) z[i] = 0u;
+        }
         if (append) {
             const int64_t slot = __ldg(slot_mapping + s);
             if (slot >= (static_cast<int64_t>(num_blocks) << bs_log2)) {
@@ -715,7 +742,8 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
                 const int32_t seg_a = prefix[wc.s] + wc.h * wc.np, seg_b = seg_a + wc.np;
                 if (seg_a >= a_w && seg_b <= b_w) {
                     // whole segment inside this warp: normalise and write out
-                    __nv_bfloat16* o = out + (static_cast<int64_t>(wc.s) * Hq + wc.h * G) * D;
+                    const int64_t row0 = static_cast<int64_t>(wc.s) * Hq + wc.h * G;
+                    __nv_bfloat16* o = out + row0 * D;
 #pragma unroll
                     for (int nh = 0; nh < NH; ++nh)
 #pragma unroll
@@ -723,6 +751,16 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
                             const int32_t head = nh * 8 + tig * 2 + hh;
                             if (head >= G) continue;
                             const float inv = 1.f / Lh[nh][hh];
+                            if (part.o != nullptr) {  // a part: normalised fp32 row, (max, sum)
+                                float* prow = part.o + (row0 + head) * D + gid;
+#pragma unroll
+                                for (int mt = 0; mt < NMT; ++mt) {
+                                    prow[mt * 16] = acc[nh][mt][hh] * inv;
+                                    prow[mt * 16 + 8] = acc[nh][mt][2 + hh] * inv;
+                                }
+                                if (gid == 0) part.ml[row0 + head] = make_float2(mh[nh][hh], Lh[nh][hh]);
+                                continue;
+                            }
                             __nv_bfloat16* orow = o + head * D + gid;
 #pragma unroll
                             for (int mt = 0; mt < NMT; ++mt) {
@@ -891,7 +929,15 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
             for (int k = 0; k < 4; ++k) {
                 const int32_t g = g0 + k;
                 if (g >= G) continue;
-                if (complete) {
+                if (complete && part.o != nullptr) {
+                    // a part: normalised fp32 row and (max, sum) (lane 0 holds them: it is one of
+                    // the lanes the reductions above reach)
+                    const int64_t row = static_cast<int64_t>(s) * Hq + h * G + g;
+                    float* dst = part.o + row * D + lane * E;
+#pragma unroll
+                    for (int e = 0; e < E; ++e) dst[e] = v[k][e];
+                    if (lane == 0) part.ml[row] = make_float2(Mk[k], dk[k]);
+                } else if (complete) {
                     uint32_t* dst =
                         reinterpret_cast<uint32_t*>(out + (static_cast<int64_t>(s) * Hq + h * G + g) * D + lane * E);
                     dst[0] = pack_bf16x2(v[k][0], v[k][1]);
@@ -919,8 +965,8 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
             tr_l3 += last ? 2 : 1;
 #endif
             if (last) {
-                merge_pieces<D>(out + (static_cast<int64_t>(s) * Hq + h * G) * D, seg_a, c_first, c_last, U, C, G, ws,
-                                lane);
+                const int64_t row0 = static_cast<int64_t>(s) * Hq + h * G;
+                merge_pieces<D>(out + row0 * D, seg_a, c_first, c_last, U, C, G, ws, lane, part, row0);
                 if (lane == 0) ws.counter[seg] = 0;
                 PA_TRACE_STAMP(g_trace, 10);
             }
@@ -978,7 +1024,8 @@ cudaError_t launch_impl(const DecodeArgs& a, const DecodePlan& plan, cudaStream_
                               a.err, static_cast<const int4*>(a.k_new), static_cast<const int4*>(a.v_new),
                               a.slot_mapping, static_cast<int4*>(const_cast<void*>(a.k_cache)),
                               static_cast<int4*>(const_cast<void*>(a.v_cache)), a.tables_ready ? 1 : 0,
-                              a.pool_ready ? 1 : 0, drill.limit_ns, drill.kind == kDrillDecodeStage ? 1 : 0);
+                              a.pool_ready ? 1 : 0, drill.limit_ns, drill.kind == kDrillDecodeStage ? 1 : 0,
+                              a.len_offset, a.part);
 }
 
 // CTAs of the NW-warp kernel that fit on one SM with `smem` bytes of dynamic shared memory

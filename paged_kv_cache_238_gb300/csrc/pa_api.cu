@@ -387,6 +387,111 @@ PA_API pa_status pa_decode(void* out, const void* q, const void* k_cache, const 
                         workspace_bytes, stream);
 }
 
+namespace {
+// Host checks of a shared-prefix decode call; fills the decode arguments and the plan.
+pa_status prepare_shared_prefix(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                int32_t num_seqs, int32_t max_seq_len, int32_t num_q_heads, int32_t num_kv_heads,
+                                int32_t head_dim, int32_t num_blocks, float scale, int32_t prefix_tokens,
+                                void* workspace, size_t workspace_bytes, DecodeArgs* a) {
+    pa_status st = prepare_decode(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens, num_seqs,
+                                  max_seq_len, num_q_heads, num_kv_heads, head_dim, num_blocks, PA_BLOCK_SIZE, scale,
+                                  PA_BF16, workspace, workspace_bytes, a);
+    if (st != PA_OK) return st;
+    if (prefix_tokens <= 0 || prefix_tokens % PA_BLOCK_SIZE != 0 || prefix_tokens > max_seq_len ||
+        prefix_tokens / PA_BLOCK_SIZE > max_blocks_per_seq)
+        return PA_ERR_INVALID_ARG;
+    const int32_t G = num_q_heads / num_kv_heads;
+    if (head_dim != 128 || (G != 4 && G != 8 && G != 16)) return PA_ERR_UNSUPPORTED;
+    if (num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
+
+// The plan of a checked shared-prefix call and the check of the workspace against it.
+pa_status plan_shared_prefix_checked(const DecodeArgs& a, int32_t prefix_tokens, const DeviceInfo& info,
+                                     SharedPrefixPlan* plan) {
+    *plan = plan_shared_prefix(a.num_seqs, a.num_q_heads, a.num_kv_heads, a.head_dim, a.max_seq_len, prefix_tokens,
+                               info);
+    if (a.num_seqs == 0) return PA_OK;
+    if (plan->dplan.path != kDecodeMmaBalanced) return PA_ERR_UNSUPPORTED;
+    if (!a.workspace || a.workspace_bytes < plan->total || !aligned16(a.workspace)) return PA_ERR_INVALID_ARG;
+    return PA_OK;
+}
+}  // namespace
+
+PA_API size_t pa_decode_shared_prefix_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                                     int32_t head_dim, int32_t max_seq_len, int32_t prefix_tokens) {
+    DecodeArgs a;
+    const void* fake = reinterpret_cast<const void*>(static_cast<uintptr_t>(0x10000));
+    if (prepare_shared_prefix(const_cast<void*>(fake), fake, fake, fake, static_cast<const int32_t*>(fake),
+                              (max_seq_len + 15) / 16 + 1, static_cast<const int32_t*>(fake), num_seqs, max_seq_len,
+                              num_q_heads, num_kv_heads, head_dim, 1, 1.f, prefix_tokens, const_cast<void*>(fake),
+                              ~static_cast<size_t>(0), &a) != PA_OK)
+        return 0;
+    DeviceCache* dev = nullptr;
+    if (device_cache(&dev) != cudaSuccess) return 0;
+    SharedPrefixPlan plan;
+    if (plan_shared_prefix_checked(a, prefix_tokens, dev->info, &plan) != PA_OK) return 0;
+    return plan.total;
+}
+
+PA_API pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                         const int32_t* block_table, int32_t max_blocks_per_seq,
+                                         const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
+                                         int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                         int32_t num_blocks, float scale, int32_t prefix_tokens, void* workspace,
+                                         size_t workspace_bytes, void* stream) {
+    DecodeArgs a;
+    pa_status st = prepare_shared_prefix(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens,
+                                         num_seqs, max_seq_len, num_q_heads, num_kv_heads, head_dim, num_blocks,
+                                         scale, prefix_tokens, workspace, workspace_bytes, &a);
+    if (st != PA_OK || num_seqs == 0) return st;
+    DeviceCache* dev = nullptr;
+    if (device_cache(&dev) != cudaSuccess) return PA_ERR_CUDA;
+    SharedPrefixPlan plan;
+    st = plan_shared_prefix_checked(a, prefix_tokens, dev->info, &plan);
+    if (st != PA_OK) return st;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char* ws = static_cast<char*>(workspace);
+    float* parts_o = reinterpret_cast<float*>(ws + plan.parts_o_off);
+    float2* parts_ml = reinterpret_cast<float2*>(ws + plan.parts_ml_off);
+    // (1) each sequence's suffix, keys [prefix_tokens, len), as fp32 parts, on a capped grid
+    a.err = dev->err;
+    a.workspace = ws;
+    a.workspace_bytes = plan.dplan.workspace_bytes;
+    a.block_table = block_table + prefix_tokens / PA_BLOCK_SIZE;
+    a.len_offset = prefix_tokens;
+    a.max_seq_len = max_seq_len - prefix_tokens;
+    a.part.o = parts_o;
+    a.part.ml = parts_ml;
+    if (launch_decode(a, plan.dplan, s) != cudaSuccess) return PA_ERR_CUDA;
+    // (2) the prefix, once per kv head: every sequence's query row over row 0's prefix blocks,
+    // merged with its suffix part into the output
+    PrefillArgs p{};
+    p.out = out;
+    p.q = q;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_table = block_table;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.num_seqs = 1;
+    p.max_chunk_len = num_seqs;
+    p.max_seq_len = prefix_tokens;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.head_dim = head_dim;
+    p.num_blocks = num_blocks;
+    p.scale = scale;
+    p.dtype = PA_BF16;
+    p.err = dev->err;
+    p.block_size = PA_BLOCK_SIZE;
+    p.sp.rows = num_seqs;
+    p.sp.len = prefix_tokens;
+    p.sp.suffix_o = parts_o;
+    p.sp.suffix_ml = parts_ml;
+    return launch_prefill(p, dev->info, s) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 PA_API pa_status pa_prefill_chunk_bs(void* out, const void* q, const void* k_cache, const void* v_cache,
                                      const int32_t* block_table, int32_t max_blocks_per_seq, const int32_t* seq_lens,
                                      const int32_t* query_start_loc, int32_t num_seqs, int32_t max_chunk_len,

@@ -48,6 +48,14 @@ cudaError_t launch_copy_blocks(const CopyBlocksArgs& a, cudaStream_t stream);
 // ------------------------------------------------------------------------------------------
 // decode
 // ------------------------------------------------------------------------------------------
+// Attention over a part of each row's keys, per row r (= sequence * H_q + q head): the
+// normalised output at o + r * D (fp32) and its (max, sum) at ml[r] (log2 domain), so that
+// parts over disjoint key ranges merge exactly by the log-sum-exp rule.
+struct PartOut {
+    float* o = nullptr;
+    float2* ml = nullptr;
+};
+
 struct DecodeArgs {
     void* out;
     const void* q;
@@ -72,6 +80,12 @@ struct DecodeArgs {
     bool tables_ready = false;
     // ... nor the pool rows this call reads (implies tables_ready)
     bool pool_ready = false;
+    // balanced path: keys [len_offset, seq_lens[i]) only (the caller's table rows begin
+    // len_offset / block_size entries before block_table; with len_offset > 0 the kernel checks
+    // that every row's first entries equal row 0's), and, with part.o set, each row's
+    // normalised fp32 output and (max, sum) instead of the bf16 output
+    int32_t len_offset = 0;
+    PartOut part;
 };
 
 // A pipeline wait gives up after this long; the kernel then raises PA_DEVERR_WAIT_TIMEOUT,
@@ -129,6 +143,20 @@ bool plan_decode_balanced(int32_t num_seqs, int32_t num_kv_heads, int32_t group,
                           const DeviceInfo& dev, DecodePlan* plan, int32_t max_ctas = 0, bool append = false);
 cudaError_t launch_decode_balanced(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream);
 
+// Decode over a prefix shared by every sequence (shared_prefix.cu): the suffixes by the
+// balanced decode kernel on a grid capped to leave prefix_ctas SMs, written as fp32 parts;
+// then the prefix by the tensor-core prefill kernel in shared-prefix mode, launched so that it
+// runs beside the decode and merges the suffix parts into the output at its end. Workspace: the
+// decode's workspace, then the suffix parts [S][H_q][D] fp32 at parts_o_off and their (max,
+// sum) [S][H_q][2] at parts_ml_off.
+struct SharedPrefixPlan {
+    int32_t prefix_ctas = 0;
+    DecodePlan dplan{};
+    size_t parts_o_off = 0, parts_ml_off = 0, total = 0;
+};
+SharedPrefixPlan plan_shared_prefix(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                    int32_t max_seq_len, int32_t prefix_tokens, const DeviceInfo& dev);
+
 // SIMT path (decode_simt.cu).
 cudaError_t launch_decode_simt(const DecodeArgs& a, const DecodePlan& plan, cudaStream_t stream);
 int simt_heads_per_cta();
@@ -136,6 +164,17 @@ int simt_heads_per_cta();
 // ------------------------------------------------------------------------------------------
 // prefill
 // ------------------------------------------------------------------------------------------
+// Tensor-core prefill in shared-prefix mode: one query row per decode sequence, all of them
+// over the same `len` prefix keys (block-table row 0), no causal bound. Each row's suffix part
+// (keys past the prefix, computed by the decode kernel launched just before) is merged in
+// before the bf16 output is written; the kernel waits for that decode grid only there.
+struct SharedPrefixPart {
+    int32_t rows = 0;  // 0: ordinary chunked prefill
+    int32_t len = 0;
+    const float* suffix_o = nullptr;    // [rows][H_q][D]
+    const float2* suffix_ml = nullptr;  // [rows][H_q]
+};
+
 struct PrefillArgs {
     void* out;
     const void* q;
@@ -150,6 +189,7 @@ struct PrefillArgs {
     pa_dtype dtype;
     uint32_t* err;
     int32_t block_size;  // tokens per block: 16, 32, 64 or 128
+    SharedPrefixPart sp;  // shared-prefix mode (tensor-core path only) when sp.rows > 0
 };
 // total_rows: number of chunk rows (query_start_loc[num_seqs]); the host cannot read it, so
 // the caller passes an upper bound (grid rows past the end exit at once).

@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
     __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ q, const int32_t* __restrict__ block_table,
     int32_t max_blocks, const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ query_start_loc,
     int32_t num_kv_heads, int32_t num_blocks, int32_t sub_log2, float scale_log2, uint32_t* err, uint64_t wait_limit_ns,
-    int32_t drill) {
+    int32_t drill, SharedPrefixPart sp) {
     constexpr int TT = kTcRows / G;  // chunk tokens per Q tile
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -133,9 +133,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
     // sequence of rank z, so the longest CTAs start first and the grid ends on short ones.
     __shared__ int32_t lpt_len[kLptMaxSeqs];
     __shared__ int32_t lpt_seq;
-    int32_t seq = blockIdx.z;
-    const int32_t n_seqs = static_cast<int32_t>(gridDim.z);
-    if (n_seqs <= kLptMaxSeqs) {
+    const bool prefix_mode = sp.rows > 0;
+    int32_t seq = prefix_mode ? 0 : blockIdx.z;
+    const int32_t n_seqs = prefix_mode ? 1 : static_cast<int32_t>(gridDim.z);
+    if (!prefix_mode && n_seqs <= kLptMaxSeqs) {
         if (tid < n_seqs) lpt_len[tid] = __ldg(seq_lens + tid);
         __syncthreads();
         if (tid < n_seqs) {
@@ -153,20 +154,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
     const int32_t h = blockIdx.y;
     const int32_t pair = gridDim.x - 1 - blockIdx.x;  // the longest pairs start first
     const int32_t Hq = G * num_kv_heads;
-    const int32_t q0 = __ldg(query_start_loc + seq);
-    const int32_t C = __ldg(query_start_loc + seq + 1) - q0;
-    const int32_t L = __ldg(seq_lens + seq);
-    const int32_t t0a = 2 * pair * TT, t0b = t0a + TT;
+    // Shared-prefix mode: the "chunk" is one query row per decode sequence (C = sp.rows) and
+    // every row sees all L = sp.len prefix keys (no causal bound).
+    const int32_t q0 = prefix_mode ? 0 : __ldg(query_start_loc + seq);
+    const int32_t C = prefix_mode ? sp.rows : __ldg(query_start_loc + seq + 1) - q0;
+    const int32_t L = prefix_mode ? sp.len : __ldg(seq_lens + seq);
+    // (shared-prefix mode: one Q tile per CTA, so that twice as many CTAs share the work)
+    const int32_t t0a = prefix_mode ? pair * TT : 2 * pair * TT, t0b = prefix_mode ? C : t0a + TT;
     if (t0a >= C) return;  // uniform over the CTA
-    if (C > L || L > table_tokens(max_blocks, sub_log2) || C < 0) {
+    if ((!prefix_mode && C > L) || L > table_tokens(max_blocks, sub_log2) || C < 0) {
         if (tid == 0) raise_error(err, PA_DEVERR_LEN_RANGE);
         return;
     }
-    const int32_t P0 = L - C;  // position of chunk row 0
+    const int32_t P0 = prefix_mode ? L - 1 : L - C;  // position of chunk row 0
     const bool active_b = t0b < C;
-    // key tiles holding keys visible to some row of each Q tile
-    const int32_t n_kv_a = (P0 + min(t0a + TT, C) - 1) / kTcKeys + 1;
-    const int32_t n_kv_b = active_b ? (P0 + min(t0b + TT, C) - 1) / kTcKeys + 1 : 0;
+    // key tiles holding keys visible to some row of each Q tile (every prefix key for every
+    // row in shared-prefix mode)
+    const int32_t n_kv_a = prefix_mode ? (L + kTcKeys - 1) / kTcKeys : (P0 + min(t0a + TT, C) - 1) / kTcKeys + 1;
+    const int32_t n_kv_b = !active_b ? 0 : prefix_mode ? n_kv_a : (P0 + min(t0b + TT, C) - 1) / kTcKeys + 1;
+    // shared-prefix mode: let the next kernel's grid be scheduled now (it waits for this one to
+    // complete before it reads anything this kernel writes)
+    if (prefix_mode) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int32_t n_kv = max(n_kv_a, n_kv_b);
     const int32_t npages = (L + kPageTokens - 1) / kPageTokens;
 
@@ -469,7 +477,42 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
             ok = wait_or_abort(&o_done[xq], 0, abort_flag, err, wait_limit_ns);
             ok = __all_sync(0xffffffffu, ok);
         }
-        if (ok && n_kv_x > 0) {
+        if (ok && n_kv_x > 0 && prefix_mode) {
+            // the row's suffix part comes from the decode grid launched before this kernel:
+            // wait for it here (every thread that reads it), then merge
+            //   M = max(m, m_s),  out = (O 2^(m - M) + l_s o_s 2^(m_s - M)) / (l 2^(m - M) + l_s 2^(m_s - M))
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            umma::fence_after_sync();
+            const int64_t prow = static_cast<int64_t>(t0 + tl) * Hq + h * G + g;
+            float2 ms = make_float2(-INFINITY, 0.f);
+            if (row_valid) ms = __ldcg(sp.suffix_ml + prow);
+            const float M = ms.y > 0.f ? fmaxf(m_ref, ms.x) : m_ref;
+            const float a = fast_exp2(m_ref - M), b = ms.y > 0.f ? ms.y * fast_exp2(ms.x - M) : 0.f;
+            const float inv = 1.f / (l_sum * a + b);
+            const float ca = a * inv, cb = b * inv;
+            const float* so = sp.suffix_o + prow * kTcD;
+            __nv_bfloat16* orow = out + prow * kTcD;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t raw[32];
+                umma::ld_32x32b_x32(tmem_o + lane_off + c * 32, raw);
+                umma::wait_ld();
+                if (row_valid) {
+#pragma unroll
+                    for (int v8 = 0; v8 < 4; ++v8) {
+                        const float4 s0 = __ldcg(reinterpret_cast<const float4*>(so + c * 32 + v8 * 8));
+                        const float4 s1 = __ldcg(reinterpret_cast<const float4*>(so + c * 32 + v8 * 8 + 4));
+                        const float* r = reinterpret_cast<const float*>(raw) + v8 * 8;
+                        uint4 w;
+                        w.x = pack_bf16x2(fmaf(r[0], ca, s0.x * cb), fmaf(r[1], ca, s0.y * cb));
+                        w.y = pack_bf16x2(fmaf(r[2], ca, s0.z * cb), fmaf(r[3], ca, s0.w * cb));
+                        w.z = pack_bf16x2(fmaf(r[4], ca, s1.x * cb), fmaf(r[5], ca, s1.y * cb));
+                        w.w = pack_bf16x2(fmaf(r[6], ca, s1.z * cb), fmaf(r[7], ca, s1.w * cb));
+                        *reinterpret_cast<uint4*>(orow + c * 32 + v8 * 8) = w;
+                    }
+                }
+            }
+        } else if (ok && n_kv_x > 0) {
             umma::fence_after_sync();
             const float inv = 1.f / l_sum;
             __nv_bfloat16* orow = out + (static_cast<int64_t>(q0 + t0 + tl) * Hq + h * G + g) * kTcD;
@@ -522,15 +565,25 @@ cudaError_t launch_tc(const PrefillArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     constexpr int TT = kTcRows / G;
     const int32_t tiles = (a.max_chunk_len + TT - 1) / TT;
-    const int32_t pairs = (tiles + 1) / 2;
-    dim3 grid(pairs, a.num_kv_heads, a.num_seqs);
+    const int32_t pairs = a.sp.rows > 0 ? tiles : (tiles + 1) / 2;  // Q tiles (pairs) per (sequence, kv head)
+    dim3 grid(pairs, a.num_kv_heads, a.sp.rows > 0 ? 1 : a.num_seqs);
     const WaitDrill drill = wait_drill();
-    prefill_tc_kernel<G><<<grid, kTcThreads, TcSmem::total, stream>>>(
-        tm_k, tm_v, static_cast<__nv_bfloat16*>(a.out), static_cast<const __nv_bfloat16*>(a.q), a.block_table,
-        a.max_blocks_per_seq, a.seq_lens, a.query_start_loc, a.num_kv_heads, a.num_blocks,
-        block_size_log2(a.block_size) - 4, a.scale * kLog2e, a.err, drill.limit_ns,
-        drill.kind == kDrillPrefillKTile ? 1 : 0);
-    return cudaGetLastError();
+    // Shared-prefix mode is a programmatic launch: its CTAs may start while the decode grid
+    // before it runs (it waits for that grid before its merge).
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = TcSmem::total;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = a.sp.rows > 0 ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, prefill_tc_kernel<G>, tm_k, tm_v, static_cast<__nv_bfloat16*>(a.out),
+                              static_cast<const __nv_bfloat16*>(a.q), a.block_table, a.max_blocks_per_seq, a.seq_lens,
+                              a.query_start_loc, a.num_kv_heads, a.num_blocks, block_size_log2(a.block_size) - 4,
+                              a.scale * kLog2e, a.err, drill.limit_ns, drill.kind == kDrillPrefillKTile ? 1 : 0, a.sp);
 }
 
 }  // namespace
@@ -549,6 +602,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, const DeviceInfo& dev, cudaStre
             default: return launch_tc<16>(a, stream);
         }
     }
+    if (a.sp.rows > 0) return cudaErrorInvalidValue;  // shared-prefix mode: tensor-core path only
     const int32_t total_rows = a.num_seqs * a.max_chunk_len;  // upper bound; extra rows exit at once
     return launch_prefill_simt(a, total_rows, stream);
 }

@@ -215,6 +215,7 @@ def build_decode(seed: int, lens, H_q: int, H_kv: int, D: int, num_blocks: int, 
     if keep_contiguous:
         wl.contiguous_k, wl.contiguous_v = ck, cv
     wl.info["blocks_used"] = int(alloc.next + 1)
+    wl.info["shared_prefix_tokens"] = int(shared_prefix_tokens)
     return wl
 
 
