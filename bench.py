@@ -931,7 +931,7 @@ def main(argv=None):
     ap.add_argument("--event-every", type=int, default=50, help="time each kernel on every Nth step of a graph")
     ap.add_argument("--preheat-s", type=float, default=1.0)
     ap.add_argument("--min-replays", type=int, default=20, help="timed replays of the K-step graph (at least)")
-    ap.add_argument("--e2e-block", type=int, default=8, help="e2e: steps per input/output copy group")
+    ap.add_argument("--e2e-block", type=int, default=4, help="e2e: steps per input/output copy group")
     ap.add_argument("--min-timed-ms", type=float, default=50.0, help="replay the K-step graph for at least this long")
     ap.add_argument("--cpu-budget-s", type=float, default=10.0)
     ap.add_argument("--reference-budget-s", type=float, default=90.0)
