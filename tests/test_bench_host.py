@@ -38,6 +38,12 @@ def test_shared_prefix_blocks_count_once_in_the_distinct_bytes():
     tok = 2 * 1 * 8 * 2
     assert b["kv"] == 120 * tok
     assert b["kv_unique"] == (32 + 3 * 8) * tok  # two shared blocks once, three private tails
+    # the decode bytes (value and roofline) count the distinct keys; the logical figure each
+    # sequence's keys
+    q = 3 * 4 * 8 * 2
+    rest = 2 * q + 4 * 3 * 3 + 4 * 3            # Q and output, 3 table entries per row, lengths
+    assert b["decode"] == b["kv_unique"] + rest
+    assert b["decode_logical"] == b["kv"] + rest
 
 
 def test_step_inputs_are_packed_and_a_second_buffer_set_mirrors_them():

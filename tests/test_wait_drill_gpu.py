@@ -131,3 +131,33 @@ def test_prefill_wait_runs_out_and_the_next_call_matches_oracle():
     ref = oracle.attention(wl.q_prefill, kc, vc, wl.block_table_prefill, wl.seq_lens_prefill, wl.scale,
                            query_start_loc=qsl)
     assert_close(to_f64(dw.out_prefill), ref, "bf16", "prefill after a drilled call")
+
+
+@pytest.mark.parametrize("kind", ["decode", "prefill"])
+def test_shared_prefix_wait_runs_out_and_the_next_call_matches_oracle(kind):
+    """pa_decode_shared_prefix runs both kernels: the drill stops one wait of the suffix decode
+    or of the prefix kernel that runs beside it; the next call matches the oracle."""
+    lens = 256 + np.array([0, 5, 40, 300, 17, 96])
+    need = 16 + int(np.sum(-(-(lens - 256) // 16))) + 2
+    wl = W.build_decode(670, lens, H_q=32, H_kv=8, D=128, num_blocks=need, dtype="bf16", new_token=False,
+                        shared_prefix_tokens=256)
+    dw = DeviceWorkload(wl)
+    msl = int(lens.max())
+    ws = torch.zeros(B.pa_decode_shared_prefix_workspace_size(wl.S, wl.H_q, wl.H_kv, wl.D, msl, 256),
+                     dtype=torch.uint8, device="cuda")
+
+    def call():
+        B.pa_decode_shared_prefix(dw.out, dw.q, dw.k_cache, dw.v_cache, dw.block_table, dw.seq_lens, msl, wl.scale,
+                                  256, ws)
+
+    drill = B.PA_DRILL_DECODE_STAGE if kind == "decode" else B.PA_DRILL_PREFILL_K_TILE
+    errs, dt = _drilled(drill, call)
+    assert errs & B.PA_DEVERR_WAIT_TIMEOUT, f"no timeout raised (errors {errs:#x})"
+    assert dt < 0.5
+    ws.zero_()
+    dw.out.fill_(float("nan"))
+    call()
+    torch.cuda.synchronize()
+    assert B.pa_get_device_errors(clear=True) == 0
+    ref = oracle.attention(wl.q, wl.k_cache, wl.v_cache, wl.block_table, wl.seq_lens, wl.scale)
+    assert_close(to_f64(dw.out), ref, "bf16", f"shared prefix after a drilled {kind} wait")
