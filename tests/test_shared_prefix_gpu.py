@@ -95,3 +95,31 @@ def test_a_row_with_other_prefix_blocks_is_flagged():
     dw, _ = _run(wl, 256)
     assert B.pa_get_device_errors(clear=True) == B.PA_DEVERR_PREFIX_MISMATCH
     assert_close(to_f64(dw.out), _ref(wl), "bf16", "copied prefix block")
+
+
+@pytest.mark.parametrize("S", [1, 3])
+def test_every_suffix_empty(S):
+    """Every sequence is exactly the shared prefix: the output is the prefix part alone."""
+    lens = np.full(S, 384)
+    wl = W.build_decode(680 + S, lens, H_q=32, H_kv=8, D=128, num_blocks=24 + 2, dtype="bf16", new_token=False,
+                        shared_prefix_tokens=384)
+    dw, _ = _run(wl, 384)
+    assert B.pa_get_device_errors(clear=True) == 0
+    assert_close(to_f64(dw.out), _ref(wl), "bf16", f"empty suffixes, S {S}")
+
+
+def test_length_shorter_than_the_prefix_is_flagged():
+    """A sequence shorter than prefix_tokens breaks the call's contract: PA_DEVERR_LEN_RANGE."""
+    lens = np.array([300, 290, 400])
+    need = 16 + int(np.sum(-(-(lens - 256) // 16))) + 2
+    wl = W.build_decode(690, lens, H_q=32, H_kv=8, D=128, num_blocks=need, dtype="bf16", new_token=False,
+                        shared_prefix_tokens=256)
+    dw = DeviceWorkload(wl)
+    msl = int(lens.max())
+    ws = torch.zeros(B.pa_decode_shared_prefix_workspace_size(wl.S, wl.H_q, wl.H_kv, wl.D, msl, 256),
+                     dtype=torch.uint8, device="cuda")
+    dw.seq_lens[1] = 200  # below the prefix
+    B.pa_decode_shared_prefix(dw.out, dw.q, dw.k_cache, dw.v_cache, dw.block_table, dw.seq_lens, msl, wl.scale, 256,
+                              ws)
+    torch.cuda.synchronize()
+    assert B.pa_get_device_errors(clear=True) & B.PA_DEVERR_LEN_RANGE
