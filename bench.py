@@ -537,7 +537,8 @@ class DeviceStep:
             rec("decode", 0)
             if self.prefix:
                 B.pa_decode_shared_prefix(T["out"], T["q"], self.kcs[r], self.vcs[r], T["bt"], T["lens"], self.msl,
-                                          wl.scale, self.prefix, self.ws, stream=s)
+                                          wl.scale, self.prefix, self.ws, stream=s, tables_ready=True,
+                                          pool_ready=self.pool_ready)
             else:
                 B.pa_decode(T["out"], T["q"], self.kcs[r], self.vcs[r], T["bt"], T["lens"], self.msl, wl.scale,
                             self.ws, stream=s)

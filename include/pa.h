@@ -193,6 +193,11 @@ PA_API pa_status pa_decode(void* out, const void* q, const void* k_cache, const 
  *   - workspace: >= pa_decode_shared_prefix_workspace_size(...) bytes, 16-byte aligned,
  *     zero-filled before its first use, under the rules of pa_decode_workspace_size (its first
  *     part is the suffix decode's workspace).
+ *   - flags: 0, or the promises PA_DECODE_TABLES_READY / PA_DECODE_POOL_READY of
+ *     pa_decode_append (below) about the kernel launched just before this call; with
+ *     POOL_READY that kernel writes no pool row of keys 0 .. seq_lens[i] - 1. They let the
+ *     suffix decode scan the lengths and start its first page copies before its wait.
+ *     Other bits: PA_ERR_INVALID_ARG.
  * No counterpart entry point exists on the source pages; they describe the sharing of the
  * blocks, and this computes on that sharing.
  */
@@ -203,7 +208,7 @@ PA_API pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k
                                          const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
                                          int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                          int32_t num_blocks, float scale, int32_t prefix_tokens, void* workspace,
-                                         size_t workspace_bytes, void* stream);
+                                         size_t workspace_bytes, uint32_t flags, void* stream);
 
 /*
  * pa_decode_append: one decode step with its new tokens, in one launch where it can be. For

@@ -99,7 +99,7 @@ def load(build_if_needed: bool = True) -> ctypes.CDLL:
             lib.pa_decode_shared_prefix_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
             lib.pa_decode_shared_prefix.restype = ctypes.c_int
             lib.pa_decode_shared_prefix.argtypes = [vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, f32, i32,
-                                                    vp, sz, vp]
+                                                    vp, sz, ctypes.c_uint32, vp]
             lib.pa_debug_set_wait_drill.restype = ctypes.c_int
             lib.pa_debug_set_wait_drill.argtypes = [i32, ctypes.c_uint64]
             i64, pi32, pi64, pu8 = (ctypes.c_int64, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64),
@@ -242,9 +242,12 @@ def pa_decode_shared_prefix_workspace_size(num_seqs: int, num_q_heads: int, num_
 
 
 def pa_decode_shared_prefix(out, q, k_cache, v_cache, block_table, seq_lens, max_seq_len: int, scale: float,
-                            prefix_tokens: int, workspace, stream=None) -> None:
+                            prefix_tokens: int, workspace, stream=None, tables_ready: bool = False,
+                            pool_ready: bool = False) -> None:
     """pa_decode for a batch whose table rows all start with the same prefix_tokens / 16 block
-    ids (C ABI pa_decode_shared_prefix): the prefix is attended once per kv head; bf16."""
+    ids (C ABI pa_decode_shared_prefix): the prefix is attended once per kv head; bf16.
+    tables_ready / pool_ready: the promises PA_DECODE_TABLES_READY / PA_DECODE_POOL_READY about
+    the kernel launched just before the call (see pa_decode_append)."""
     _need_cuda(out, q, k_cache, v_cache, block_table, seq_lens, workspace)
     S, H_q, D = q.shape
     NB, H_kv = k_cache.shape[0], k_cache.shape[1]
@@ -252,7 +255,8 @@ def pa_decode_shared_prefix(out, q, k_cache, v_cache, block_table, seq_lens, max
     _check("pa_decode_shared_prefix", load().pa_decode_shared_prefix(
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
         _ptr(seq_lens), S, int(max_seq_len), H_q, H_kv, D, NB, float(scale), int(prefix_tokens), _ptr(workspace),
-        ws_bytes, _stream(stream)))
+        ws_bytes, (PA_DECODE_TABLES_READY if tables_ready else 0) | (PA_DECODE_POOL_READY if pool_ready else 0),
+        _stream(stream)))
 
 
 def pa_decode_bs(out, q, k_cache, v_cache, block_table, seq_lens, max_seq_len: int, scale: float,

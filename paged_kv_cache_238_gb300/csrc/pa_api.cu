@@ -440,7 +440,8 @@ PA_API pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k
                                          const int32_t* seq_lens, int32_t num_seqs, int32_t max_seq_len,
                                          int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                          int32_t num_blocks, float scale, int32_t prefix_tokens, void* workspace,
-                                         size_t workspace_bytes, void* stream) {
+                                         size_t workspace_bytes, uint32_t flags, void* stream) {
+    if (flags & ~static_cast<uint32_t>(PA_DECODE_TABLES_READY | PA_DECODE_POOL_READY)) return PA_ERR_INVALID_ARG;
     DecodeArgs a;
     pa_status st = prepare_shared_prefix(out, q, k_cache, v_cache, block_table, max_blocks_per_seq, seq_lens,
                                          num_seqs, max_seq_len, num_q_heads, num_kv_heads, head_dim, num_blocks,
@@ -464,6 +465,8 @@ PA_API pa_status pa_decode_shared_prefix(void* out, const void* q, const void* k
     a.max_seq_len = max_seq_len - prefix_tokens;
     a.part.o = parts_o;
     a.part.ml = parts_ml;
+    a.pool_ready = (flags & PA_DECODE_POOL_READY) != 0;
+    a.tables_ready = a.pool_ready || (flags & PA_DECODE_TABLES_READY) != 0;
     if (launch_decode(a, plan.dplan, s) != cudaSuccess) return PA_ERR_CUDA;
     // (2) the prefix, once per kv head: every sequence's query row over row 0's prefix blocks,
     // merged with its suffix part into the output

@@ -59,7 +59,7 @@ struct TcSmem {
     static constexpr uint32_t k = q + 2 * kTile;              // kKStages stages
     static constexpr uint32_t v = k + kKStages * kTile;       // kVStages stages
     static constexpr uint32_t bars = v + kVStages * kTile;
-    static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 8;
+    static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 9;
     static constexpr uint32_t misc = bars + kNumBars * 8;     // tmem base, abort flag
     static constexpr uint32_t total = misc + 16 + 1024;
 };
@@ -123,6 +123,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
     uint64_t* o_done = p_full + 2;                 // [2] last PV of Q tile a / b finished (commit)
     uint64_t* q_full = o_done + 2;                 // Q tiles stored in shared memory (256 threads)
     uint64_t* idle = q_full + 1;                   // every MMA issued has finished (final commit)
+    uint64_t* ml_full = idle + 1;                  // shared-prefix mode: both tiles' (max, sum) stored
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + TcSmem::misc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + TcSmem::misc + 4);
 
@@ -159,23 +160,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
     const int32_t q0 = prefix_mode ? 0 : __ldg(query_start_loc + seq);
     const int32_t C = prefix_mode ? sp.rows : __ldg(query_start_loc + seq + 1) - q0;
     const int32_t L = prefix_mode ? sp.len : __ldg(seq_lens + seq);
-    // (shared-prefix mode: one Q tile per CTA, so that twice as many CTAs share the work)
-    const int32_t t0a = prefix_mode ? pair * TT : 2 * pair * TT, t0b = prefix_mode ? C : t0a + TT;
+    // Shared-prefix mode: one Q tile per CTA, held in both Q slots; its key tiles alternate
+    // between the slots (even tiles: a, odd tiles: b), so that both softmax warpgroups and the
+    // tensor core's interleaving serve the one tile, and the two parts merge at the end.
+    const int32_t t0a = prefix_mode ? pair * TT : 2 * pair * TT, t0b = prefix_mode ? t0a : t0a + TT;
     if (t0a >= C) return;  // uniform over the CTA
     if ((!prefix_mode && C > L) || L > table_tokens(max_blocks, sub_log2) || C < 0) {
         if (tid == 0) raise_error(err, PA_DEVERR_LEN_RANGE);
         return;
     }
     const int32_t P0 = prefix_mode ? L - 1 : L - C;  // position of chunk row 0
-    const bool active_b = t0b < C;
-    // key tiles holding keys visible to some row of each Q tile (every prefix key for every
-    // row in shared-prefix mode)
-    const int32_t n_kv_a = prefix_mode ? (L + kTcKeys - 1) / kTcKeys : (P0 + min(t0a + TT, C) - 1) / kTcKeys + 1;
-    const int32_t n_kv_b = !active_b ? 0 : prefix_mode ? n_kv_a : (P0 + min(t0b + TT, C) - 1) / kTcKeys + 1;
+    const int32_t n_prefix_tiles = (L + kTcKeys - 1) / kTcKeys;  // shared-prefix mode
+    const bool active_b = prefix_mode ? n_prefix_tiles > 1 : t0b < C;
+    // key tiles of each slot: those holding keys visible to some row of its Q tile; in
+    // shared-prefix mode every prefix tile, split between the slots
+    const int32_t n_kv_a = prefix_mode ? (n_prefix_tiles + 1) / 2 : (P0 + min(t0a + TT, C) - 1) / kTcKeys + 1;
+    const int32_t n_kv_b = !active_b ? 0 : prefix_mode ? n_prefix_tiles / 2 : (P0 + min(t0b + TT, C) - 1) / kTcKeys + 1;
     // shared-prefix mode: let the next kernel's grid be scheduled now (it waits for this one to
     // complete before it reads anything this kernel writes)
     if (prefix_mode) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int32_t n_kv = max(n_kv_a, n_kv_b);
+    const int32_t n_kv = prefix_mode ? n_prefix_tiles : max(n_kv_a, n_kv_b);  // key tiles produced
     const int32_t npages = (L + kPageTokens - 1) / kPageTokens;
 
     if (tid == 0) {
@@ -184,6 +188,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
         mbar_init(&p_full[0], 4);
         mbar_init(&p_full[1], 4);
         mbar_init(q_full, kSoftmaxThreads);
+        mbar_init(ml_full, kSoftmaxThreads);
         fence_mbarrier_init();
     }
     if (warp == kMmaWarp) {
@@ -306,14 +311,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
             if (leader) umma::commit(&s_full[x]);
             __syncwarp();
         };
-        auto pv = [&](int32_t x, int32_t j) {
+        // O_x += P_x V(j); `acc` false: the first PV of slot x overwrites O_x
+        auto pv = [&](int32_t x, int32_t j, bool acc) {
             const uint64_t dv = dv0 + static_cast<uint64_t>(j % kVStages) * (kTile >> 4);
             const uint32_t a_p = tmem + x * 128, d_o = tmem + 256 + x * 128;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {  // 16 keys per instruction: 8 P columns
                 if (leader)
                     umma::mma_bf16_tmem_a(d_o, a_p + kk * 8, dv + static_cast<uint64_t>(kk * (2048 >> 4)), idesc_pv,
-                                          (j > 0 || kk > 0));
+                                          (acc || kk > 0));
             }
             __syncwarp();
         };
@@ -324,19 +330,54 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
             return ok;
         };
         bool ok = wait_or_abort(q_full, 0, abort_flag, err, wait_limit_ns) && wait_k(0);
-        if (ok) {
+        if (prefix_mode) {
+            // key tile i: slot i & 1, K and V stages i % kKStages, i % kVStages; per tile
+            //   PV_x(i), QK_x(i + 2)
+            // so the slots alternate on the tensor core like two Q tiles do
+            if (ok) {
+                qk(0, 0);
+                if (leader) umma::commit(&k_empty[0]);
+            }
+            if (ok && n_kv > 1) {
+                ok = wait_k(1);
+                if (ok) {
+                    qk(1, 1);
+                    if (leader) umma::commit(&k_empty[1 % kKStages]);
+                }
+            }
+            for (int32_t i = 0; i < n_kv && ok; ++i) {
+                const int32_t x = i & 1;
+                ok = wait_or_abort(&v_full[i % kVStages], static_cast<uint32_t>(i / kVStages) & 1u, abort_flag, err,
+                                   wait_limit_ns);
+                if (ok) ok = wait_or_abort(&p_full[x], static_cast<uint32_t>(i >> 1) & 1u, abort_flag, err, wait_limit_ns);
+                umma::fence_after_sync();
+                if (ok) pv(x, i, i >= 2);
+                if (ok && leader) {
+                    umma::commit(&v_empty[i % kVStages]);
+                    if (i + 2 >= n_kv) umma::commit(&o_done[x]);
+                }
+                if (ok && i + 2 < n_kv) {
+                    ok = wait_k(i + 2);
+                    if (ok) {
+                        qk(x, i + 2);
+                        if (leader) umma::commit(&k_empty[(i + 2) % kKStages]);
+                    }
+                }
+                __syncwarp();
+            }
+        } else if (ok) {
             qk(0, 0);
             if (active_b) qk(1, 0);
             if (leader) umma::commit(&k_empty[0]);
         }
-        for (int32_t j = 0; j < n_kv && ok; ++j) {
+        for (int32_t j = 0; j < n_kv && ok && !prefix_mode; ++j) {
             const bool ua = j < n_kv_a, ub = j < n_kv_b;
             const bool ua1 = j + 1 < n_kv_a, ub1 = j + 1 < n_kv_b;
             ok = wait_or_abort(&v_full[j % kVStages], static_cast<uint32_t>(j / kVStages) & 1u, abort_flag, err, wait_limit_ns);
             if (ok && ua) {
                 ok = wait_or_abort(&p_full[0], j & 1, abort_flag, err, wait_limit_ns);  // P_a(j) written, S_a(j) read
                 umma::fence_after_sync();
-                if (ok) pv(0, j);
+                if (ok) pv(0, j, j > 0);
                 if (ok && !ua1 && leader) umma::commit(&o_done[0]);
             }
             if (ok && (ua1 || ub1)) ok = wait_k(j + 1);
@@ -344,7 +385,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
             if (ok && ub) {
                 ok = wait_or_abort(&p_full[1], j & 1, abort_flag, err, wait_limit_ns);
                 umma::fence_after_sync();
-                if (ok) pv(1, j);
+                if (ok) pv(1, j, j > 0);
                 if (ok && !ub1 && leader) umma::commit(&o_done[1]);
             }
             if (ok && leader) umma::commit(&v_empty[j % kVStages]);
@@ -373,7 +414,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
                 break;
             }
             umma::fence_after_sync();
-            const int32_t kbase = j * kTcKeys;
+            const int32_t kt = prefix_mode ? 2 * j + xq : j;  // key tile of this step
+            const int32_t kbase = kt * kTcKeys;
             const bool diag = kbase + kTcKeys - 1 > pos;  // only these tiles need the causal mask
             // pass 1: row max of the raw scores (scale > 0), eight independent chains
             float mxk[8];
@@ -455,10 +497,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
             }
             m_ref = m_new;
             // keys of this tile past the sequence end: zero their V rows (thread r: key row r),
-            // by the first Q tile that uses key tile j
-            if ((xq == 0 || j >= n_kv_a) && kbase + r >= L) {
-                const int32_t st = j % kVStages;
-                const bool okv = wait_or_abort(&v_full[st], static_cast<uint32_t>(j / kVStages) & 1u, abort_flag, err, wait_limit_ns);
+            // by the first Q tile that uses key tile kt (the only one in shared-prefix mode)
+            if ((prefix_mode || xq == 0 || j >= n_kv_a) && kbase + r >= L) {
+                const int32_t st = kt % kVStages;
+                const bool okv = wait_or_abort(&v_full[st], static_cast<uint32_t>(kt / kVStages) & 1u, abort_flag, err,
+                                               wait_limit_ns);
                 if (okv) {
                     uint8_t* sv_tile = smem + TcSmem::v + st * kTile;
 #pragma unroll
@@ -473,46 +516,78 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[xq]);
         }
-        if (ok && n_kv_x > 0) {
-            ok = wait_or_abort(&o_done[xq], 0, abort_flag, err, wait_limit_ns);
+        if (prefix_mode) {
+            // Both slots' last PVs have finished once o_done of each has: then every MMA of the
+            // CTA has, and the Q slots are free to carry the slots' (max, sum) per row.
+            if (ok) ok = wait_or_abort(&o_done[0], 0, abort_flag, err, wait_limit_ns);
+            if (ok && active_b) ok = wait_or_abort(&o_done[1], 0, abort_flag, err, wait_limit_ns);
             ok = __all_sync(0xffffffffu, ok);
-        }
-        if (ok && n_kv_x > 0 && prefix_mode) {
-            // the row's suffix part comes from the decode grid launched before this kernel:
-            // wait for it here (every thread that reads it), then merge
-            //   M = max(m, m_s),  out = (O 2^(m - M) + l_s o_s 2^(m_s - M)) / (l 2^(m - M) + l_s 2^(m_s - M))
-            asm volatile("griddepcontrol.wait;" ::: "memory");
-            umma::fence_after_sync();
-            const int64_t prow = static_cast<int64_t>(t0 + tl) * Hq + h * G + g;
-            float2 ms = make_float2(-INFINITY, 0.f);
-            if (row_valid) ms = __ldcg(sp.suffix_ml + prow);
-            const float M = ms.y > 0.f ? fmaxf(m_ref, ms.x) : m_ref;
-            const float a = fast_exp2(m_ref - M), b = ms.y > 0.f ? ms.y * fast_exp2(ms.x - M) : 0.f;
-            const float inv = 1.f / (l_sum * a + b);
-            const float ca = a * inv, cb = b * inv;
-            const float* so = sp.suffix_o + prow * kTcD;
-            __nv_bfloat16* orow = out + prow * kTcD;
+            float2* mls = reinterpret_cast<float2*>(smem + TcSmem::q);  // [slot][row]
+            if (ok) mls[xq * kTcRows + r] = make_float2(m_ref, l_sum);
+            mbar_arrive(ml_full);  // every softmax thread, so that no wait below is left hanging
+            if (ok) ok = wait_or_abort(ml_full, 0, abort_flag, err, wait_limit_ns);
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok) {
+                // The row's three parts: the prefix keys of slot a and of slot b (unnormalised
+                // O_x under max m_x, sum l_x) and its suffix part from the decode grid launched
+                // before this kernel (normalised o_s, m_s, l_s), which is waited for here:
+                //   M = max(m_a, m_b, m_s),  w_x = 2^(m_x - M),  w_s = l_s 2^(m_s - M)
+                //   out = (w_a O_a + w_b O_b + w_s o_s) / (w_a l_a + w_b l_b + w_s)
+                // Slot a's warpgroup writes columns 0-63 of the row, slot b's 64-127.
+                asm volatile("griddepcontrol.wait;" ::: "memory");
+                umma::fence_after_sync();
+                const int64_t prow = static_cast<int64_t>(t0 + tl) * Hq + h * G + g;
+                const float2 pa = mls[r];
+                const float2 pb = active_b ? mls[kTcRows + r] : make_float2(-INFINITY, 0.f);
+                float2 ms = make_float2(-INFINITY, 0.f);
+                if (row_valid) ms = __ldcg(sp.suffix_ml + prow);
+                float M = pa.x;
+                if (active_b) M = fmaxf(M, pb.x);
+                if (ms.y > 0.f) M = fmaxf(M, ms.x);
+                const float wa = fast_exp2(pa.x - M);
+                const float wb = active_b ? fast_exp2(pb.x - M) : 0.f;
+                const float wsuf = ms.y > 0.f ? ms.y * fast_exp2(ms.x - M) : 0.f;
+                const float inv = 1.f / (pa.y * wa + pb.y * wb + wsuf);
+                const float ca = wa * inv, cb = wb * inv, cs = wsuf * inv;
+                const float* so = sp.suffix_o + prow * kTcD;
+                __nv_bfloat16* orow = out + prow * kTcD;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t raw[32];
-                umma::ld_32x32b_x32(tmem_o + lane_off + c * 32, raw);
-                umma::wait_ld();
-                if (row_valid) {
+                for (int half = 0; half < 2; ++half) {
+                    const int32_t c = 2 * xq + half;  // 32-column chunk
+                    uint32_t ra[32], rb[32];
+                    umma::ld_32x32b_x32(tmem + 256 + lane_off + c * 32, ra);
+                    if (active_b) umma::ld_32x32b_x32(tmem + 256 + 128 + lane_off + c * 32, rb);
+                    umma::wait_ld();
+                    if (!active_b) {
 #pragma unroll
-                    for (int v8 = 0; v8 < 4; ++v8) {
-                        const float4 s0 = __ldcg(reinterpret_cast<const float4*>(so + c * 32 + v8 * 8));
-                        const float4 s1 = __ldcg(reinterpret_cast<const float4*>(so + c * 32 + v8 * 8 + 4));
-                        const float* r = reinterpret_cast<const float*>(raw) + v8 * 8;
-                        uint4 w;
-                        w.x = pack_bf16x2(fmaf(r[0], ca, s0.x * cb), fmaf(r[1], ca, s0.y * cb));
-                        w.y = pack_bf16x2(fmaf(r[2], ca, s0.z * cb), fmaf(r[3], ca, s0.w * cb));
-                        w.z = pack_bf16x2(fmaf(r[4], ca, s1.x * cb), fmaf(r[5], ca, s1.y * cb));
-                        w.w = pack_bf16x2(fmaf(r[6], ca, s1.z * cb), fmaf(r[7], ca, s1.w * cb));
-                        *reinterpret_cast<uint4*>(orow + c * 32 + v8 * 8) = w;
+                        for (int i = 0; i < 32; ++i) rb[i] = 0u;
+                    }
+                    if (row_valid) {
+#pragma unroll
+                        for (int v8 = 0; v8 < 4; ++v8) {
+                            const float4 s0 = __ldcg(reinterpret_cast<const float4*>(so + c * 32 + v8 * 8));
+                            const float4 s1 = __ldcg(reinterpret_cast<const float4*>(so + c * 32 + v8 * 8 + 4));
+                            const float sv[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+                            float o8[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                o8[e] = fmaf(__uint_as_float(ra[v8 * 8 + e]), ca,
+                                             fmaf(__uint_as_float(rb[v8 * 8 + e]), cb, sv[e] * cs));
+                            uint4 w;
+                            w.x = pack_bf16x2(o8[0], o8[1]);
+                            w.y = pack_bf16x2(o8[2], o8[3]);
+                            w.z = pack_bf16x2(o8[4], o8[5]);
+                            w.w = pack_bf16x2(o8[6], o8[7]);
+                            *reinterpret_cast<uint4*>(orow + c * 32 + v8 * 8) = w;
+                        }
                     }
                 }
             }
         } else if (ok && n_kv_x > 0) {
+            ok = wait_or_abort(&o_done[xq], 0, abort_flag, err, wait_limit_ns);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        if (!prefix_mode && ok && n_kv_x > 0) {
             umma::fence_after_sync();
             const float inv = 1.f / l_sum;
             __nv_bfloat16* orow = out + (static_cast<int64_t>(q0 + t0 + tl) * Hq + h * G + g) * kTcD;

@@ -264,6 +264,7 @@ def test_wait_drill_arguments_are_checked_on_the_host():
     (dict(Hq=16, Hkv=8), B.PA_ERR_UNSUPPORTED),         # 2 q heads per kv head
     (dict(D=64), B.PA_ERR_UNSUPPORTED),                 # head_dim 64
     (dict(dt_ok=False), B.PA_ERR_INVALID_ARG),          # unaligned output
+    (dict(flags=4), B.PA_ERR_INVALID_ARG),              # unknown flag bit
 ])
 def test_shared_prefix_decode_rejects_bad_arguments(kw, expect):
     """Host checks of pa_decode_shared_prefix, made before anything touches a device."""
@@ -271,5 +272,5 @@ def test_shared_prefix_decode_rejects_bad_arguments(kw, expect):
     S, Hq, Hkv, D, msl = 4, kw.get("Hq", 32), kw.get("Hkv", 8), kw.get("D", 128), kw.get("msl", 2048)
     out = FAKE if kw.get("dt_ok", True) else FAKE + 2
     st = lib.pa_decode_shared_prefix(out, FAKE, FAKE, FAKE, FAKE, msl // 16, FAKE, S, msl, Hq, Hkv, D, 4096,
-                                     ctypes.c_float(0.1), kw.get("prefix", 1024), FAKE, 1 << 30, None)
+                                     ctypes.c_float(0.1), kw.get("prefix", 1024), FAKE, 1 << 30, kw.get("flags", 0), None)
     assert st == expect

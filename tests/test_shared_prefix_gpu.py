@@ -79,6 +79,25 @@ def test_workspace_reuse_gives_identical_results():
     assert_close(to_f64(dw.out), _ref(wl), "bf16", "workspace reuse")
 
 
+def test_ready_flags_give_the_same_bits():
+    """With PA_DECODE_TABLES_READY / PA_DECODE_POOL_READY (the kernel before each call is the
+    previous call's prefix kernel, which writes neither the tables nor the pool) the suffix
+    decode starts earlier; the results are bit for bit those of the call without flags."""
+    wl = W.prefix_sharing()
+    dw, ws = _run(wl, 1024)
+    plain = to_host_bits(dw.out).copy()
+    msl = int(wl.seq_lens.max())
+    for tables_ready, pool_ready in ((True, False), (False, True), (True, True)):
+        dw.out.fill_(float("nan"))
+        for _ in range(3):  # back to back: each call's kernels follow the previous call's
+            B.pa_decode_shared_prefix(dw.out, dw.q, dw.k_cache, dw.v_cache, dw.block_table, dw.seq_lens, msl,
+                                      wl.scale, 1024, ws, tables_ready=tables_ready, pool_ready=pool_ready)
+        torch.cuda.synchronize()
+        assert B.pa_get_device_errors(clear=True) == 0
+        assert np.array_equal(to_host_bits(dw.out), plain), (tables_ready, pool_ready)
+    assert_close(to_f64(dw.out), _ref(wl), "bf16", "shared-prefix decode with ready flags")
+
+
 def test_a_row_with_other_prefix_blocks_is_flagged():
     """Row 3's second prefix block is replaced by a copy of it in another physical block: the
     values are the same, so the output still matches, but the table breaks the call's contract
