@@ -102,6 +102,15 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
     return d;
 }
 
+// 16-byte copy global -> shared (cp.async, L2 only); with `zero` the 16 bytes are zeros and the
+// source is not read.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* src, bool zero) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)), "l"(src),
+                 "r"(zero ? 0 : 16)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 template <int G>
 __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -182,6 +191,47 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
     const int32_t n_kv = prefix_mode ? n_prefix_tiles : max(n_kv_a, n_kv_b);  // key tiles produced
     const int32_t npages = (L + kPageTokens - 1) / kPageTokens;
 
+    // tensor memory columns: S of Q tile x at 128 x (fp32; its P, bf16 pairs, overwrites the
+    // first 64 columns once read), O of Q tile x at 256 + 128 x (fp32)
+    const bool softmax_warp = warp >= kSoftWarp0 && warp < kVWarp;
+    const int32_t xq = softmax_warp ? (warp - kSoftWarp0) >> 2 : 0;  // Q tile of a softmax warp
+    const int32_t t0 = xq ? t0b : t0a;
+    if (softmax_warp) {
+        // ---- Q tiles, by the softmax threads, started before the barriers and the tensor
+        // memory are set up: row r = token * G + head, 16-byte copies into the swizzled K-major
+        // layout (two 64-column halves); rows past the chunk are zero
+        const int32_t ti = tid - 32 * kSoftWarp0 - xq * 128;  // thread within its warpgroup
+        uint8_t* sq = smem + TcSmem::q + xq * kTile;
+        constexpr int kPer = kTcRows * 16 / 128;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int32_t i = ti + k * 128;
+            const int32_t r = i >> 4, c16 = i & 15;  // row, 16-byte chunk of the 256-byte row
+            const int32_t t = t0 + r / G, g = r % G;
+            const bool in = t < C;
+            const __nv_bfloat16* src = in ? q + (static_cast<int64_t>(q0 + t) * Hq + h * G + g) * kTcD + c16 * 8 : q;
+            cp_async16(sq + (c16 >> 3) * kHalf + sw128_offset(r, c16 & 7), src, !in);
+        }
+    }
+    // block ids, 32 pages (four key tiles) per window: lane i of a producer warp holds page
+    // 32 w + i; the first two windows are fetched before the barriers are set up
+    auto page_row = [&](int32_t pg) -> int32_t {
+        int32_t phys = 0;  // keys past the sequence end read the null block; masked later
+        if (pg < npages) {
+            phys = __ldg(block_table + static_cast<int64_t>(seq) * max_blocks + (pg >> sub_log2));
+            if (phys < 0 || phys >= num_blocks) {
+                raise_error(err, PA_DEVERR_BLOCK_RANGE);
+                phys = 0;
+            }
+        }
+        return (((phys * num_kv_heads + h) << sub_log2) + (pg & ((1 << sub_log2) - 1))) * kPageTokens;
+    };
+    int32_t row_cur = 0, row_nxt = 0;
+    if (warp == kKWarp || warp == kVWarp) {
+        row_cur = page_row(lane);
+        row_nxt = page_row(32 + lane);
+    }
+
     if (tid == 0) {
         *abort_flag = 0;
         for (int i = 0; i < TcSmem::kNumBars; ++i) mbar_init(&bars[i], 1);
@@ -199,34 +249,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
     __syncthreads();  // barriers initialised, tensor memory allocated: the producers start now
     umma::fence_after_sync();
     const uint32_t tmem = *tmem_holder;
-    // tensor memory columns: S of Q tile x at 128 x (fp32; its P, bf16 pairs, overwrites the
-    // first 64 columns once read), O of Q tile x at 256 + 128 x (fp32)
-    const bool softmax_warp = warp >= kSoftWarp0 && warp < kVWarp;
-    const int32_t xq = softmax_warp ? (warp - kSoftWarp0) >> 2 : 0;  // Q tile of a softmax warp
-    const int32_t t0 = xq ? t0b : t0a;
     if (softmax_warp) {
-        // ---- Q tiles, by the softmax threads while the first K/V copies are in flight: row
-        // r = token * G + head, 16-byte loads (all issued before any store) into the swizzled
-        // K-major layout (two 64-column halves); rows past the chunk are zero
-        const int32_t ti = tid - 32 * kSoftWarp0 - xq * 128;  // thread within its warpgroup
-        uint8_t* sq = smem + TcSmem::q + xq * kTile;
-        constexpr int kPer = kTcRows * 16 / 128;
-        int4 v[kPer];
-#pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-            const int32_t i = ti + k * 128;
-            const int32_t r = i >> 4, c16 = i & 15;  // row, 16-byte chunk of the 256-byte row
-            const int32_t t = t0 + r / G, g = r % G;
-            v[k] = make_int4(0, 0, 0, 0);
-            if (t < C) v[k] = *reinterpret_cast<const int4*>(q + (static_cast<int64_t>(q0 + t) * Hq + h * G + g) * kTcD + c16 * 8);
-        }
-#pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-            const int32_t i = ti + k * 128;
-            const int32_t r = i >> 4, c16 = i & 15;
-            *reinterpret_cast<int4*>(sq + (c16 >> 3) * kHalf + sw128_offset(r, c16 & 7)) = v[k];
-        }
-        fence_proxy_async_shared();  // generic stores before the tensor core reads them
+        cp_async_wait_all();         // this thread's Q copies have landed
+        fence_proxy_async_shared();  // before the tensor core reads them
         mbar_arrive(q_full);
     }
 
@@ -242,21 +267,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
         uint64_t* empty = is_v ? v_empty : k_empty;
         uint8_t* ring = smem + (is_v ? TcSmem::v : TcSmem::k);
         if (lane == 0) prefetch_tensormap(tm);
-        // block ids, 32 pages (four key tiles) per window: lane i holds page 32 w + i; the
-        // next window is fetched while the current one is issued
-        auto page_row = [&](int32_t pg) -> int32_t {
-            int32_t phys = 0;  // keys past the sequence end read the null block; masked later
-            if (pg < npages) {
-                phys = __ldg(block_table + static_cast<int64_t>(seq) * max_blocks + (pg >> sub_log2));
-                if (phys < 0 || phys >= num_blocks) {
-                    raise_error(err, PA_DEVERR_BLOCK_RANGE);
-                    phys = 0;
-                }
-            }
-            return (((phys * num_kv_heads + h) << sub_log2) + (pg & ((1 << sub_log2) - 1))) * kPageTokens;
-        };
+        // the next window of block ids is fetched while the current one is issued
         int32_t win = 0;
-        int32_t row_cur = page_row(lane), row_nxt = page_row(32 + lane);
         // With the wait drill on, one CTA's K producer announces 16 bytes more for its first
         // tile than the copies bring: that tile never completes and the MMA warp's wait runs out.
         const uint32_t drill_bytes = (drill && warp == kKWarp && pair == 0 && h == 0 && blockIdx.z == 0) ? 16u : 0u;
