@@ -142,12 +142,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
     // sequences go in order of decreasing total length (ties by index): CTA z takes the
     // sequence of rank z, so the longest CTAs start first and the grid ends on short ones.
     __shared__ int32_t lpt_len[kLptMaxSeqs];
+    __shared__ int32_t lpt_qsl[kLptMaxSeqs + 1];  // the chunk starts, read with the lengths
     __shared__ int32_t lpt_seq;
     const bool prefix_mode = sp.rows > 0;
     int32_t seq = prefix_mode ? 0 : blockIdx.z;
     const int32_t n_seqs = prefix_mode ? 1 : static_cast<int32_t>(gridDim.z);
-    if (!prefix_mode && n_seqs <= kLptMaxSeqs) {
+    const bool lpt = !prefix_mode && n_seqs <= kLptMaxSeqs;
+    if (lpt) {
         if (tid < n_seqs) lpt_len[tid] = __ldg(seq_lens + tid);
+        if (tid <= n_seqs) lpt_qsl[tid] = __ldg(query_start_loc + tid);
         __syncthreads();
         if (tid < n_seqs) {
             const int32_t mine = lpt_len[tid];
@@ -166,9 +169,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) prefill_tc_kernel(
     const int32_t Hq = G * num_kv_heads;
     // Shared-prefix mode: the "chunk" is one query row per decode sequence (C = sp.rows) and
     // every row sees all L = sp.len prefix keys (no causal bound).
-    const int32_t q0 = prefix_mode ? 0 : __ldg(query_start_loc + seq);
-    const int32_t C = prefix_mode ? sp.rows : __ldg(query_start_loc + seq + 1) - q0;
-    const int32_t L = prefix_mode ? sp.len : __ldg(seq_lens + seq);
+    const int32_t q0 = prefix_mode ? 0 : lpt ? lpt_qsl[seq] : __ldg(query_start_loc + seq);
+    const int32_t C = prefix_mode ? sp.rows : (lpt ? lpt_qsl[seq + 1] : __ldg(query_start_loc + seq + 1)) - q0;
+    const int32_t L = prefix_mode ? sp.len : lpt ? lpt_len[seq] : __ldg(seq_lens + seq);
     // Shared-prefix mode: one Q tile per CTA, held in both Q slots; its key tiles alternate
     // between the slots (even tiles: a, odd tiles: b), so that both softmax warpgroups and the
     // tensor core's interleaving serve the one tile, and the two parts merge at the end.
