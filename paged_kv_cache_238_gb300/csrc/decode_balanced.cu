@@ -4,10 +4,11 @@
 // Work list. The unit of work is one (sequence, kv head, logical block) page: 16 tokens x
 // head_dim of K plus the same of V (8 KB at head_dim 128). Units are ordered sequence-major,
 // then kv head, then page, so the units of one (sequence, kv head) "segment" are contiguous.
-// Every CTA rebuilds the list's prefix sums from seq_lens with a block-wide scan and takes an
-// equal contiguous slice of it (one persistent CTA per SM); inside the CTA each warp takes an
-// equal contiguous sub-slice. Per-SM work differs by at most one page whatever the mix of
-// lengths.
+// Every CTA rebuilds the list's prefix sums from seq_lens with a block-wide scan and takes a
+// contiguous slice of it (one persistent CTA per SM); inside the CTA each warp takes an equal
+// contiguous sub-slice. The slices are equal to within one page whatever the mix of lengths,
+// except that the last tenth of the CTAs, which start last when launches overlap, get a fixed
+// number of pages fewer (Slices).
 //
 // Streaming. Each warp is an independent worker with its own ring of stages in shared memory.
 // Lane 0 resolves a page's physical block through the block table ("My Understanding of vLLM
@@ -55,6 +56,7 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kBalMaxGroup = 16;
 constexpr int kBalMaxSeqs = 1024;  // per-sequence tables live in shared memory
+constexpr uint32_t kLightBytes = 96u * 1024u;  // K/V bytes fewer for each of the last CTAs
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
@@ -118,12 +120,40 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
-// First unit of slice c when U units are cut into C equal contiguous slices.
-__host__ __device__ __forceinline__ int64_t slice_start(int64_t c, int64_t U, int64_t C) { return c * U / C; }
-// The slice that holds unit u (the last one among slices that start at or before u).
-__host__ __device__ __forceinline__ int64_t slice_owner(int64_t u, int64_t U, int64_t C) {
-    return ((u + 1) * C + U - 1) / U - 1;
-}
+// The work list's U units cut into C contiguous slices, one per CTA. With programmatic
+// launches a grid's CTAs take the SMs in index order as the previous grid's CTAs leave them, so
+// the highest-indexed CTAs start last, up to a few microseconds after the first ones. The last
+// K CTAs (from cb = C - K on) therefore get d units fewer than the others: with A = U + K d,
+// slice c starts at floor((c A - C max(0, c - cb) d) / C). Light slices are used only when each
+// of them keeps at least one unit (U - cb d >= C); otherwise the slices are equal (K = d = 0).
+struct Slices {
+    int64_t U, A;
+    int32_t C, cb, d;
+    __device__ __forceinline__ void init(int64_t u, int32_t c, int32_t light, int32_t deficit) {
+        U = u;
+        C = c;
+        cb = c - light;
+        d = deficit;
+        if (light <= 0 || light >= c || deficit <= 0 || u - static_cast<int64_t>(cb) * deficit < c) {
+            cb = c;
+            d = 0;
+        }
+        A = U + static_cast<int64_t>(C - cb) * d;
+    }
+    // first unit of slice c
+    __device__ __forceinline__ int64_t start(int64_t c) const {
+        const int64_t light = c > cb ? c - cb : 0;
+        return (c * A - static_cast<int64_t>(C) * light * d) / C;
+    }
+    // the slice that holds unit u (the last one among slices that start at or before u)
+    __device__ __forceinline__ int32_t owner(int64_t u) const {
+        const int64_t c1 = ((u + 1) * C + A - 1) / A - 1;  // the answer if it is a full slice
+        if (c1 < cb) return static_cast<int32_t>(c1);
+        const int64_t den = U - static_cast<int64_t>(cb) * d;
+        const int64_t c2 = ((u + 1 - static_cast<int64_t>(cb) * d) * C + den - 1) / den - 1;
+        return static_cast<int32_t>(c2 < C - 1 ? c2 : C - 1);
+    }
+};
 
 // Sequence s with prefix[s] <= u < prefix[s + 1].
 __device__ __forceinline__ int32_t find_seq(const int32_t* prefix, int32_t S, int32_t u) {
@@ -190,12 +220,11 @@ __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity, uint6
 // partial outputs) is issued before any is used, and a running maximum folds the batches:
 //   M' = max(M, m_j),  den = den 2^(M - M') + sum_j l_j 2^(m_j - M'),  acc likewise with o_j.
 template <int D>
-__device__ __forceinline__ void merge_pieces(__nv_bfloat16* o, int32_t a, int32_t w_first, int32_t w_last, int64_t U,
-                                             int64_t W, int32_t G, const BalWorkspace& ws, int32_t lane,
+__device__ __forceinline__ void merge_pieces(__nv_bfloat16* o, int32_t first_slot, int32_t w_first, int32_t w_last,
+                                             int64_t U, int64_t W, int32_t G, const BalWorkspace& ws, int32_t lane,
                                              const PartOut& part, int64_t row0) {
     constexpr int E = D / 32;
-    const bool may_be_empty = U < W;
-    const int32_t first_slot = slice_start(w_first, U, W) < a ? 1 : 0;
+    const bool may_be_empty = U < W;  // then the slices are equal
     for (int32_t g0 = 0; g0 < G; g0 += 4) {
         float M[4], den[4], acc[4][E];
 #pragma unroll
@@ -212,7 +241,7 @@ __device__ __forceinline__ void merge_pieces(__nv_bfloat16* o, int32_t a, int32_
             for (int j = 0; j < 4; ++j) {
                 const int32_t w = w0 + j;
                 bool ok = w <= w_last;
-                if (ok && may_be_empty) ok = slice_start(w, U, W) < slice_start(w + 1, U, W);
+                if (ok && may_be_empty) ok = w * U / W < (w + 1) * U / W;
                 const int64_t piece = static_cast<int64_t>(w) * 2 + (w == w_first ? first_slot : 0);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
@@ -292,7 +321,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
     uint32_t* err, const int4* __restrict__ k_new, const int4* __restrict__ v_new,
     const int64_t* __restrict__ slot_mapping, int4* __restrict__ k_pool, int4* __restrict__ v_pool,
     int32_t tables_ready, int32_t pool_ready, uint64_t wait_limit_ns, int32_t drill, int32_t len_offset,
-    PartOut part) {
+    PartOut part, int32_t light_ctas, int32_t light_units) {
     constexpr uint32_t kPage = kPageTokens * D * 2;
     constexpr uint32_t kHalves = D / 64;
     constexpr int KS = D / 16;  // k-steps over head_dim
@@ -433,8 +462,13 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
             }
         }
     }
-    const int32_t u0 = static_cast<int32_t>(slice_start(blockIdx.x, U, C));
-    const int32_t u1 = static_cast<int32_t>(slice_start(blockIdx.x + 1, U, C));
+    int32_t u0, u1;
+    {
+        Slices sl;
+        sl.init(U, static_cast<int32_t>(C), light_ctas, light_units);
+        u0 = static_cast<int32_t>(sl.start(blockIdx.x));
+        u1 = static_cast<int32_t>(sl.start(blockIdx.x + 1));
+    }
     if (u0 >= u1) return;  // uniform over the CTA
     const int32_t n_cta = u1 - u0;
     const int32_t a_w = u0 + static_cast<int32_t>((static_cast<int64_t>(warp) * n_cta) / NW);
@@ -952,8 +986,10 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
         }
         if (!complete) {
             // ---- level 3: count this CTA's piece; the last one merges all CTA pieces ----------
-            const int32_t c_first = static_cast<int32_t>(slice_owner(seg_a, U, C));
-            const int32_t c_last = static_cast<int32_t>(slice_owner(seg_b - 1, U, C));
+            Slices sl;
+            sl.init(prefix[S], static_cast<int32_t>(gridDim.x), light_ctas, light_units);
+            const int32_t c_first = sl.owner(seg_a);
+            const int32_t c_last = sl.owner(seg_b - 1);
             const int32_t expected = (U >= C) ? (c_last - c_first + 1) : (seg_b - seg_a);
             __syncwarp();  // the warp's piece stores precede lane 0's release below
             int32_t last = 0;
@@ -966,7 +1002,8 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_balanced_kernel(
 #endif
             if (last) {
                 const int64_t row0 = static_cast<int64_t>(s) * Hq + h * G;
-                merge_pieces<D>(out + row0 * D, seg_a, c_first, c_last, U, C, G, ws, lane, part, row0);
+                const int32_t first_slot = sl.start(c_first) < seg_a ? 1 : 0;  // the segment's piece in c_first
+                merge_pieces<D>(out + row0 * D, first_slot, c_first, c_last, U, C, G, ws, lane, part, row0);
                 if (lane == 0) ws.counter[seg] = 0;
                 PA_TRACE_STAMP(g_trace, 10);
             }
@@ -1025,7 +1062,7 @@ cudaError_t launch_impl(const DecodeArgs& a, const DecodePlan& plan, cudaStream_
                               a.slot_mapping, static_cast<int4*>(const_cast<void*>(a.k_cache)),
                               static_cast<int4*>(const_cast<void*>(a.v_cache)), a.tables_ready ? 1 : 0,
                               a.pool_ready ? 1 : 0, drill.limit_ns, drill.kind == kDrillDecodeStage ? 1 : 0,
-                              a.len_offset, a.part);
+                              a.len_offset, a.part, plan.light_ctas, plan.light_units);
 }
 
 // CTAs of the NW-warp kernel that fit on one SM with `smem` bytes of dynamic shared memory
@@ -1077,6 +1114,10 @@ bool plan_decode_balanced(int32_t S, int32_t Hkv, int32_t G, int32_t D, const De
             plan->smem_bytes = L.total;
             plan->num_ctas = dev.num_sms * per_sm;
             if (max_ctas > 0 && plan->num_ctas > max_ctas) plan->num_ctas = max_ctas;
+            // The CTAs that start last (about one in ten) get fewer pages: about as many as
+            // an SM streams in the couple of microseconds by which they trail the first ones.
+            plan->light_ctas = plan->num_ctas / 10;
+            plan->light_units = static_cast<int32_t>(kLightBytes / (2u * kPageTokens * D * 2u));
             plan->workspace_bytes = bal_ws_bytes(S, Hkv, G, D, plan->num_ctas);
             return true;
         }

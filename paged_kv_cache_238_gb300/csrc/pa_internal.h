@@ -117,6 +117,8 @@ struct DecodePlan {
     int32_t stages;            // balanced: ring stages per warp
     uint32_t stage_bytes;      // balanced: bytes per stage (K page, V page, query rows)
     uint32_t smem_bytes;       // balanced: dynamic shared memory per CTA
+    int32_t light_ctas;        // balanced: the last light_ctas CTAs (the last to start) get
+    int32_t light_units;       //   light_units pages fewer than the others
     size_t workspace_bytes;
 };
 
