@@ -427,6 +427,20 @@ PA_API pa_status pa_get_device_errors(uint32_t* errors, int32_t clear);
 #define PA_DRILL_PREFILL_K_TILE 2
 PA_API pa_status pa_debug_set_wait_drill(int32_t kind, uint64_t limit_ns);
 
+/*
+ * pa_debug_decode_slices: a test hook with no counterpart in the source pages; host only, no
+ * device call. The bf16 grouped decode kernel cuts its work list of `units` (sequence, kv head,
+ * 16-token page) units into `ctas` contiguous slices, one per CTA, and its last `light_ctas`
+ * CTAs (the ones that start last when launches overlap) get `light_units` units fewer than the
+ * others, when every slice still gets a unit; otherwise the slices are equal. This writes the
+ * first unit of each slice to starts[0..ctas] (starts[ctas] = units) and, if `owners` is not
+ * null, the slice that holds unit u to owners[u] for u < units, computed by the same code as
+ * the kernel's. Errors: PA_ERR_INVALID_ARG for units outside [0, 2^31), ctas < 1 or a null
+ * `starts`. Both arrays belong to the caller.
+ */
+PA_API pa_status pa_debug_decode_slices(int64_t units, int32_t ctas, int32_t light_ctas, int32_t light_units,
+                                        int64_t* starts, int32_t* owners);
+
 /* pa_status_string: static, human-readable name of a status code. */
 PA_API const char* pa_status_string(pa_status status);
 

@@ -32,7 +32,7 @@ EXPORTED = ("pa_reshape_and_cache", "pa_decode_workspace_size", "pa_decode", "pa
             "pa_copy_blocks", "pa_reshape_and_cache_bs", "pa_decode_bs", "pa_prefill_chunk_bs",
             "pa_copy_blocks_bs", "pa_step", "pa_decode_append", "pa_bm_create_bs",
             "pa_bm_num_blocks_for_memory_bs", "pa_debug_set_wait_drill", "pa_decode_shared_prefix_workspace_size",
-            "pa_decode_shared_prefix")
+            "pa_decode_shared_prefix", "pa_debug_decode_slices")
 #: block sizes the *_bs entry points accept
 BLOCK_SIZES = (16, 32, 64, 128)
 #: size of the library's fixed scratch used by pa_decode_noalloc
@@ -102,6 +102,8 @@ def load(build_if_needed: bool = True) -> ctypes.CDLL:
                                                     vp, sz, ctypes.c_uint32, vp]
             lib.pa_debug_set_wait_drill.restype = ctypes.c_int
             lib.pa_debug_set_wait_drill.argtypes = [i32, ctypes.c_uint64]
+            lib.pa_debug_decode_slices.restype = ctypes.c_int
+            lib.pa_debug_decode_slices.argtypes = [ctypes.c_int64, i32, i32, i32, vp, vp]
             i64, pi32, pi64, pu8 = (ctypes.c_int64, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64),
                                     ctypes.POINTER(ctypes.c_uint8))
             for name, res, args in (
@@ -332,6 +334,20 @@ def pa_debug_set_wait_drill(kind: int, limit_ns: int = 0) -> None:
     """Test hook: make one bounded wait of the named kernel run out (PA_DRILL_*), with
     limit_ns as those kernels' wait limit; PA_DRILL_OFF restores normal operation."""
     _check("pa_debug_set_wait_drill", load().pa_debug_set_wait_drill(int(kind), int(limit_ns)))
+
+
+def pa_debug_decode_slices(units: int, ctas: int, light_ctas: int, light_units: int, owners: bool = True):
+    """Test hook (host only): the bf16 grouped decode kernel's slices of `units` work units over
+    `ctas` CTAs, the last `light_ctas` of them `light_units` units shorter. Returns (starts,
+    owners): the first unit of each slice (ctas + 1 entries) and the slice of each unit (or
+    None)."""
+    starts = (ctypes.c_int64 * (int(ctas) + 1))()
+    own = (ctypes.c_int32 * max(int(units), 1))() if owners else None
+    _check("pa_debug_decode_slices",
+           load().pa_debug_decode_slices(int(units), int(ctas), int(light_ctas), int(light_units),
+                                         ctypes.cast(starts, ctypes.c_void_p),
+                                         ctypes.cast(own, ctypes.c_void_p) if own is not None else None))
+    return list(starts), (list(own)[:int(units)] if own is not None else None)
 
 
 def pa_prefill_chunk_bs(out, q, k_cache, v_cache, block_table, seq_lens, query_start_loc, max_chunk_len: int,

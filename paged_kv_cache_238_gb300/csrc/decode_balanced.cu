@@ -129,7 +129,7 @@ __device__ __forceinline__ float fast_exp2(float x) {
 struct Slices {
     int64_t U, A;
     int32_t C, cb, d;
-    __device__ __forceinline__ void init(int64_t u, int32_t c, int32_t light, int32_t deficit) {
+    __host__ __device__ __forceinline__ void init(int64_t u, int32_t c, int32_t light, int32_t deficit) {
         U = u;
         C = c;
         cb = c - light;
@@ -141,12 +141,12 @@ struct Slices {
         A = U + static_cast<int64_t>(C - cb) * d;
     }
     // first unit of slice c
-    __device__ __forceinline__ int64_t start(int64_t c) const {
+    __host__ __device__ __forceinline__ int64_t start(int64_t c) const {
         const int64_t light = c > cb ? c - cb : 0;
         return (c * A - static_cast<int64_t>(C) * light * d) / C;
     }
     // the slice that holds unit u (the last one among slices that start at or before u)
-    __device__ __forceinline__ int32_t owner(int64_t u) const {
+    __host__ __device__ __forceinline__ int32_t owner(int64_t u) const {
         const int64_t c1 = ((u + 1) * C + A - 1) / A - 1;  // the answer if it is a full slice
         if (c1 < cb) return static_cast<int32_t>(c1);
         const int64_t den = U - static_cast<int64_t>(cb) * d;
@@ -1154,6 +1154,19 @@ cudaError_t launch_decode_balanced(const DecodeArgs& a, const DecodePlan& plan, 
 }
 
 }  // namespace pa
+
+// Test hook: the balanced decode kernel's slices of `units` work units over `ctas` CTAs, as the
+// kernel computes them (host copy of the same arithmetic).
+extern "C" PA_API pa_status pa_debug_decode_slices(int64_t units, int32_t ctas, int32_t light_ctas, int32_t light_units,
+                                                   int64_t* starts, int32_t* owners) {
+    if (units < 0 || units > INT32_MAX || ctas < 1 || starts == nullptr) return PA_ERR_INVALID_ARG;
+    pa::Slices sl;
+    sl.init(units, ctas, light_ctas, light_units);
+    for (int32_t c = 0; c <= ctas; ++c) starts[c] = sl.start(c);
+    if (owners != nullptr && units > 0)
+        for (int64_t u = 0; u < units; ++u) owners[u] = sl.owner(u);
+    return PA_OK;
+}
 
 #ifdef PA_TRACE
 // Profiling builds only: copy the timeline ring to the host / clear it (current device).
